@@ -1,0 +1,92 @@
+// internal.h -- host-side declarations shared by the sffn translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <utility>
+
+#include "../../include/sffn.h"
+
+namespace sffn {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+
+// SM count of the current device (cached per device).
+int device_sm_count();
+// Opt a kernel into more than 48 KB of dynamic shared memory (once per device).
+cudaError_t set_max_smem(const void *kernel, int bytes);
+
+// Launch with programmatic stream serialisation (PDL) so the kernel may begin
+// while its predecessor drains; kernels call griddepcontrol.wait before they
+// touch any memory written earlier in the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------------------------
+// Decode
+// ---------------------------------------------------------------------------
+
+struct DecodePlan {
+    int nb;       // tokens
+    int d, F;
+    int C, R;     // gate kernel: C CTAs, each owning R consecutive neurons (a "chunk")
+    int G2;       // up/down kernel CTAs (one partial output per CTA)
+    int nlists;   // nb per-token lists (+1 union list when nb > 1)
+    int list_u;   // index of the list the up/down kernel walks
+    // workspace offsets (bytes)
+    size_t off_err, off_cnt, off_lidx, off_aeff, off_uval, off_score, off_mask, off_part, total;
+};
+
+DecodePlan make_decode_plan(int B, int d, int F);
+
+struct DecodeCall {
+    const void *x;
+    const sffn_ffn_weights *w;
+    int B, mode, score;
+    float param;
+    void *out;
+    int32_t *active_idx, *n_active;
+    void *ws;
+    float *scores_only;  // non-null: sffn_gate_scores (write scores, nothing else)
+};
+
+sffn_status run_decode(const DecodeCall &c, const DecodePlan &p, cudaStream_t s);
+sffn_status run_down_norms(const sffn_ffn_weights *w, float *norms, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Token selection / prefill
+// ---------------------------------------------------------------------------
+
+struct SelectPlan {
+    int L, d;
+    size_t off_err, off_norms, total;
+};
+SelectPlan make_select_plan(int L, int d);
+sffn_status run_token_select(const void *y_attn, int L, int d, float mass_thresh, int recent_n, int min_keep,
+                             int32_t *sel_idx, int32_t *n_sel, void *ws, const SelectPlan &p, cudaStream_t s);
+
+struct PrefillPlan {
+    int L, d, F;
+    size_t off_err, off_ysel, off_h, total;
+};
+PrefillPlan make_prefill_plan(int L, int d, int F);
+sffn_status run_prefill(const void *x, const void *y_attn, int L, const sffn_ffn_weights *w, const int32_t *sel_idx,
+                        const int32_t *n_sel, void *out, void *ws, const PrefillPlan &p, cudaStream_t s);
+
+}  // namespace sffn

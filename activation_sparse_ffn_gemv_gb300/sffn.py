@@ -1,0 +1,204 @@
+"""ctypes binding over libsffn.so (include/sffn.h) -- argument marshalling only.
+
+PyTorch supplies device memory and streams: tensors are passed as raw device
+pointers and the current torch stream is the launch stream.  Every step of the
+computation runs in the library's CUDA kernels; if the library has not been
+built (``__graft_entry__.build()`` or ``python -m
+activation_sparse_ffn_gemv_gb300.build``) the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libsffn.so")
+
+# enums (include/sffn.h)
+OK, ERR_INVALID_ARG, ERR_SHAPE, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, ERR_DEVICE = range(9)
+MODE_EXACT, MODE_THRESHOLD, MODE_KEEP_RATIO = 0, 1, 2
+ACT_RELU, ACT_SILU = 0, 1
+F32, BF16, INT4_G64 = 0, 1, 2
+SCORE_GATE, SCORE_GATE_UP = 0, 1
+WS_DECODE, WS_SELECT, WS_PREFILL = 0, 1, 2
+
+_WDTYPE = {"f32": F32, "bf16": BF16, "int4_g64": INT4_G64}
+_ACT = {"relu": ACT_RELU, "silu": ACT_SILU}
+
+
+class SffnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class FFNWeights(C.Structure):
+    _fields_ = [("wdtype", C.c_int32), ("act", C.c_int32), ("d_model", C.c_int32), ("d_ff", C.c_int32),
+                ("w_gate", C.c_void_p), ("w_up", C.c_void_p), ("w_downT", C.c_void_p),
+                ("s_gate", C.c_void_p), ("s_up", C.c_void_p), ("s_downT", C.c_void_p),
+                ("b_gate", C.c_void_p), ("down_norms", C.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libsffn.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = C.CDLL(LIB_PATH)
+        P, I, F, S = C.c_void_p, C.c_int, C.c_float, C.c_size_t
+        W = C.POINTER(FFNWeights)
+        L.sffn_status_string.argtypes = [I]
+        L.sffn_status_string.restype = C.c_char_p
+        L.sffn_workspace_size.argtypes = [I, I, W]
+        L.sffn_workspace_size.restype = S
+        L.sffn_down_norms.argtypes = [W, P, P]
+        L.sffn_down_norms.restype = I
+        L.sffn_decode.argtypes = [P, I, W, I, I, F, P, P, P, P, S, P]
+        L.sffn_decode.restype = I
+        L.sffn_gate_scores.argtypes = [P, I, W, I, P, P, S, P]
+        L.sffn_gate_scores.restype = I
+        L.sffn_token_select.argtypes = [P, I, I, F, I, I, P, P, P, S, P]
+        L.sffn_token_select.restype = I
+        L.sffn_prefill.argtypes = [P, P, I, W, P, P, P, P, S, P]
+        L.sffn_prefill.restype = I
+        L.sffn_read_device_error.argtypes = [P, C.POINTER(C.c_int32), P]
+        L.sffn_read_device_error.restype = I
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().sffn_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != OK:
+        raise SffnError(st, where)
+
+
+class Weights:
+    """One FFN layer on the device: keeps the tensors alive and the C struct."""
+
+    def __init__(self, layer: dict, down_norms: torch.Tensor | None = None):
+        self.layer = layer
+        self.d_model, self.d_ff = int(layer["d_model"]), int(layer["d_ff"])
+        self.wdtype, self.act = layer["wdtype"], layer["act"]
+        self.down_norms = down_norms
+        self.c = FFNWeights(_WDTYPE[self.wdtype], _ACT[self.act], self.d_model, self.d_ff,
+                            _ptr(layer["w_gate"]), _ptr(layer["w_up"]), _ptr(layer["w_downT"]),
+                            _ptr(layer.get("s_gate")), _ptr(layer.get("s_up")), _ptr(layer.get("s_downT")),
+                            _ptr(layer.get("b_gate")), _ptr(down_norms))
+
+    def set_down_norms(self, norms: torch.Tensor):
+        self.down_norms = norms
+        self.c.down_norms = _ptr(norms)
+
+    def ref(self):
+        return C.byref(self.c)
+
+
+def workspace_size(which: int, n: int, w: Weights | None) -> int:
+    return int(lib().sffn_workspace_size(int(which), int(n), None if w is None else w.ref()))
+
+
+def alloc_workspace(which: int, n: int, w: Weights | None, device=None) -> torch.Tensor:
+    nbytes = workspace_size(which, n, w)
+    if nbytes == 0:
+        raise SffnError(ERR_INVALID_ARG, "workspace_size")
+    # torch's caching allocator returns >= 512-byte aligned blocks
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def down_norms(w: Weights, norms: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    if norms is None:
+        norms = torch.empty(w.d_ff, dtype=torch.float32, device="cuda")
+    _check(lib().sffn_down_norms(w.ref(), _ptr(norms), _stream(stream)), "sffn_down_norms")
+    return norms
+
+
+def decode(x: torch.Tensor, w: Weights, mode: int, score: int = SCORE_GATE, param: float = 0.0,
+           out=None, active_idx=None, n_active=None, workspace=None, stream=None):
+    """Returns (out [B, d], active_idx [B, d_ff] int32, n_active [B] int32)."""
+    B = x.shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    if active_idx is None:
+        active_idx = torch.empty((B, w.d_ff), dtype=torch.int32, device=x.device)
+    if n_active is None:
+        n_active = torch.empty(B, dtype=torch.int32, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(WS_DECODE, B, w, x.device)
+    st = lib().sffn_decode(_ptr(x), B, w.ref(), int(mode), int(score), float(param), _ptr(out),
+                           _ptr(active_idx), _ptr(n_active), _ptr(workspace), workspace.numel(),
+                           _stream(stream))
+    _check(st, "sffn_decode")
+    return out, active_idx, n_active
+
+
+def gate_scores(x: torch.Tensor, w: Weights, score: int = SCORE_GATE, scores=None, workspace=None, stream=None):
+    B = x.shape[0]
+    if scores is None:
+        scores = torch.empty((B, w.d_ff), dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(WS_DECODE, B, w, x.device)
+    st = lib().sffn_gate_scores(_ptr(x), B, w.ref(), int(score), _ptr(scores), _ptr(workspace),
+                                workspace.numel(), _stream(stream))
+    _check(st, "sffn_gate_scores")
+    return scores
+
+
+def token_select(y_attn: torch.Tensor, mass_thresh: float, recent_n: int, min_keep: int,
+                 sel_idx=None, n_sel=None, workspace=None, stream=None):
+    L, d = y_attn.shape
+    if sel_idx is None:
+        sel_idx = torch.empty(L, dtype=torch.int32, device=y_attn.device)
+    if n_sel is None:
+        n_sel = torch.empty(1, dtype=torch.int32, device=y_attn.device)
+    if workspace is None:
+        workspace = alloc_workspace(WS_SELECT, L, None, y_attn.device)
+    st = lib().sffn_token_select(_ptr(y_attn), L, d, float(mass_thresh), int(recent_n), int(min_keep),
+                                 _ptr(sel_idx), _ptr(n_sel), _ptr(workspace), workspace.numel(),
+                                 _stream(stream))
+    _check(st, "sffn_token_select")
+    return sel_idx, n_sel
+
+
+def prefill(x: torch.Tensor, y_attn: torch.Tensor, w: Weights, sel_idx: torch.Tensor, n_sel: torch.Tensor,
+            out=None, workspace=None, stream=None):
+    L = x.shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    if workspace is None:
+        workspace = alloc_workspace(WS_PREFILL, L, w, x.device)
+    st = lib().sffn_prefill(_ptr(x), _ptr(y_attn), L, w.ref(), _ptr(sel_idx), _ptr(n_sel), _ptr(out),
+                            _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "sffn_prefill")
+    return out
+
+
+def read_device_error(workspace: torch.Tensor, stream=None) -> int:
+    code = C.c_int32(0)
+    _check(lib().sffn_read_device_error(_ptr(workspace), C.byref(code), _stream(stream)),
+           "sffn_read_device_error")
+    return int(code.value)

@@ -1,0 +1,348 @@
+#!/usr/bin/env python3
+"""Benchmark of the activation-sparse gated FFN on one or more GB300s.
+
+Default workload (N=1): Llama-2-7B-shaped ReGLU FFN decode (d_model 4096,
+d_ff 11008, bf16 weights, fp32 accumulation, exact gating, batch 1 token per
+call), 1024 tokens per step rotating over 8 independent layer copies (2.2 GB of
+weights, far larger than L2, so no L2 flush is needed).  A step is one CUDA
+graph of 1024 sffn_decode calls (gate -> sparse up/down -> reduce each).
+
+Prints one JSON line (rank 0).  `value` is decode microseconds per token over
+all ranks' tokens (lower is better).  `--impl reference` times the fp64 CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-FFN µs/token & HBM GB/s vs active fraction; sparse-prefill tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            hbm = d.get("hbm_gbs") or d.get("hbm_GBps")
+            bf = d.get("bf16_tflops")
+            bfs = d.get("bf16_tflops_sustained") or bf
+            if hbm:
+                return float(hbm), float(bf or FALLBACK_BF16_TFLOPS), float(bfs or FALLBACK_BF16_TFLOPS), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and self.uuid not in parts[1] and parts[1] not in self.uuid:
+                continue
+            rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[6:10]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": float(rows[0][3]) if rows[0][3].replace(".", "").isdigit() else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__ as G
+    G.build()
+    from activation_sparse_ffn_gemv_gb300 import sffn
+    from activation_sparse_ffn_gemv_gb300 import workloads as W
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    cfg = W.CONFIGS[2]
+    d, F, nlayers, T = cfg["d_model"], cfg["d_ff"], cfg["layers"], args.tokens
+    dev = torch.device("cuda", local)
+    layers = [W.make_ffn_layer(2, seed=1000 * rank, layer=l, device=dev) for l in range(nlayers)]
+    ws_list = [sffn.Weights(L) for L in layers]
+    x = W.make_tokens(2, T, seed=rank, device=dev)
+    out = torch.empty_like(x)
+    idx = torch.empty((T, F), dtype=torch.int32, device=dev)
+    nact = torch.empty(T, dtype=torch.int32, device=dev)
+    work = sffn.alloc_workspace(sffn.WS_DECODE, 1, ws_list[0], dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def enqueue(xin, oo):
+        for t in range(T):
+            sffn.decode(xin[t:t + 1], ws_list[t % nlayers], sffn.MODE_EXACT, out=oo[t:t + 1],
+                        active_idx=idx[t:t + 1], n_active=nact[t:t + 1], workspace=work, stream=stream)
+
+    with torch.cuda.stream(stream):
+        enqueue(x, out)                      # eager warm-up: sets kernel attributes before capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        enqueue(x, out)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop() if clocks else None
+    ms = e0.elapsed_time(e1)
+    ms_max = ms
+    if dist is not None:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_max = float(t.item())
+
+    # end to end: host buffers in, host buffers out, copies inside the timed region
+    xh = x.cpu().pin_memory()
+    outh = torch.empty_like(xh).pin_memory()
+    nh = torch.empty(T, dtype=torch.int32).pin_memory()
+    xd = torch.empty_like(x)
+    od = torch.empty_like(out)
+    graph_e2e = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        enqueue(xd.copy_(xh), od)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph_e2e, stream=stream):
+        enqueue(xd, od)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            xd.copy_(xh, non_blocking=True)
+            graph_e2e.replay()
+            outh.copy_(od, non_blocking=True)
+            nh.copy_(nact, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for _ in range(args.steps):
+            xd.copy_(xh, non_blocking=True)
+            graph_e2e.replay()
+            outh.copy_(od, non_blocking=True)
+            nh.copy_(nact, non_blocking=True)
+        f1.record(stream)
+    f1.synchronize()
+    ms_e2e = f0.elapsed_time(f1)
+    if dist is not None:
+        t = torch.tensor([ms_e2e], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    # active fraction and algorithmic bytes per token
+    n_np = nact.cpu().numpy().astype(np.float64)
+    a = float(n_np.mean() / F)
+    r = 2.0 * d
+    bytes_tok = (F * r + 2.0 * n_np.mean() * r      # gate rows + active up rows + active down rows
+                 + 4.0 * F                            # gate bias
+                 + 2.0 * d + 2.0 * d                  # x in, out
+                 + 4.0 * n_np.mean() + 4.0)           # active index list + count
+    us_tok = ms_max * 1e3 / (args.steps * T)
+    total_tokens = args.steps * T * world
+    value = ms_max * 1e3 / total_tokens
+    hbm, bf16_peak, bf16_sus, peak_src = peaks()
+    achieved = bytes_tok / (us_tok * 1e-6) / 1e9
+    kernels_per_call = 3
+    res = None
+    if rank == 0:
+        res = {
+            "metric": METRIC, "value": round(value, 4), "unit": "us/token", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1/d_in) weights, gate bias N(-1.2,0.3), x N(0,1)",
+            "config": {"workload": "llama2-7b-reglu-decode: d_model 4096, d_ff 11008, bf16, exact gating, "
+                                   "batch 1, 1024 tokens/step over 8 layer copies",
+                       "d_model": d, "d_ff": F, "batch": 1, "tokens_per_step": T, "layer_copies": nlayers,
+                       "mode": "exact", "l2": "inputs larger than L2: 2.2 GB of weights rotated, no flush",
+                       "parallelism": f"replicas x{world}"},
+            "active_fraction": round(a, 5),
+            "gbps": round(achieved, 1),
+            "roofline": {"bound": "hbm", "kernel": "sffn_decode call (gate + sparse up/down + reduce)",
+                         "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(achieved / hbm, 4), "peak_source": peak_src,
+                         "bytes_per_launch": round(bytes_tok), "traffic": None},
+            "e2e": {"value": round(ms_e2e * 1e3 / total_tokens, 4), "unit": "us/token",
+                    "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
+                    "d2h_bytes_per_step": int(outh.numel() * outh.element_size() + nh.numel() * 4)},
+            "gpu_launches": int(args.steps * T * kernels_per_call),
+            "clocks": clk,
+        }
+    # CPU baseline: the oracle on a bounded sample of the same workload
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(layers[0], x[: args.cpu_tokens].cpu())
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return res
+
+
+def cpu_baseline(layer_dev, x_cpu, nthreads=None):
+    import oracle as O
+    from tests.oracle_io import ffn_from_layer, mat_from_act
+    layer = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in layer_dev.items()}
+    nthreads = nthreads or os.cpu_count() or 1
+    ffn, xm = ffn_from_layer(layer), mat_from_act(x_cpu)
+    t0 = time.perf_counter()
+    O.decode(ffn, xm, O.EXACT, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    n = x_cpu.shape[0]
+    return {"value": round(dt * 1e6 / n, 1), "unit": "us/token", "cores": int(nthreads), "kind": "oracle",
+            "sample": f"{n} tokens of the same workload (layer copy 0), exact gating, fp64 oracle, "
+                      f"{nthreads} threads over tokens"}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, timed on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return None
+    import torch
+
+    import oracle as O
+    from activation_sparse_ffn_gemv_gb300 import workloads as W
+    from tests.oracle_io import ffn_from_layer, mat_from_act
+    O.build()
+    cfg = W.CONFIGS[2]
+    layer = W.make_ffn_layer(2, seed=0, layer=0)
+    nthreads = os.cpu_count() or 1
+    per_step = max(1, min(nthreads, 16))
+    x = W.make_tokens(2, per_step * (args.warmup + args.steps), seed=0)
+    ffn = ffn_from_layer(layer)
+    for i in range(args.warmup):
+        O.decode(ffn, mat_from_act(x[i * per_step:(i + 1) * per_step]), O.EXACT, nthreads=nthreads)
+    t0 = time.perf_counter()
+    for i in range(args.warmup, args.warmup + args.steps):
+        O.decode(ffn, mat_from_act(x[i * per_step:(i + 1) * per_step]), O.EXACT, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    us_tok = dt * 1e6 / (args.steps * per_step)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(us_tok, 1), "unit": "us/token", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1/d_in) weights, gate bias N(-1.2,0.3), x N(0,1)",
+        "config": {"workload": "llama2-7b-reglu-decode: d_model 4096, d_ff 11008, bf16, exact gating, "
+                               "batch 1, bounded sample per step",
+                   "d_model": cfg["d_model"], "d_ff": cfg["d_ff"], "batch": 1, "tokens_per_step": per_step},
+        "cpu_baseline": {"value": round(us_tok, 1), "unit": "us/token", "cores": nthreads, "kind": "oracle",
+                         "sample": f"{per_step} tokens per step, layer copy 0, fp64 oracle"},
+        "e2e": {"value": round(us_tok, 1), "unit": "us/token", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=1024)
+    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

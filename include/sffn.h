@@ -1,0 +1,169 @@
+/*
+ * sffn.h -- C ABI of libsffn.so: the activation-sparse gated FFN on one GB300
+ * (sm_103a).
+ *
+ * The layer computed is the gated FFN
+ *
+ *     out = W_down . ( act(W_gate . x + b) (.) (W_up . x) )
+ *
+ * where intermediate neuron j owns row j of W_gate, row j of W_up and column j
+ * of W_down (denseflux, "skipping most of a dense FFN", sec. 1 Motivation).
+ * Two ways of skipping work are provided:
+ *
+ *   decode  -- per token, only the W_up rows and W_down columns of the *active*
+ *              neurons are read.  Active means act(g_j) != 0 (exact ReLU/ReGLU
+ *              gating, denseflux sec. 5.1-5.2), or a weight-aware score
+ *              score_j = |a_j| * ||W_down[:, j]||_2 at or above a threshold, or
+ *              among the top floor(F * keep_ratio) scores (WiSparse write-up,
+ *              kwkr.cn/news/623085, sec. 1.2, 2.3 and 3.2).
+ *   prefill -- token-selective FFN: tokens are chosen by the L2 norm of their
+ *              attention-output row up to a cumulative mass threshold, the last
+ *              recent_n tokens and at least min_keep tokens are always kept, and
+ *              only the chosen tokens run the FFN; the rest pass through the
+ *              residual with Z = 0 (RedKnot token-selective sparse FFN,
+ *              bhfrc.com/news/43276, Algorithm 1 and its selection rules).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument except `w` (a host struct) and `code` in
+ *    sffn_read_device_error is a DEVICE pointer on the current CUDA device.
+ *    The caller owns all memory and the stream; the library never allocates
+ *    or frees on these calls: scratch memory comes from the caller's
+ *    `workspace` (size from sffn_workspace_size, 256-byte aligned).
+ *  - Calls are asynchronous and stream-ordered on `stream` (NULL = the legacy
+ *    default stream); nothing is read back to the host, so a sequence of calls
+ *    can be captured in a CUDA graph.  Counts (n_active, n_sel) stay on the
+ *    device.  Consecutive kernels use programmatic dependent launch.
+ *  - Argument errors are detected on the host before anything is launched and
+ *    returned as a status; a failed launch returns SFFN_ERR_CUDA.  Contract
+ *    violations that only the device can see (an out-of-range selected-token
+ *    index, n_sel > L) are recorded in an error word at the start of the
+ *    workspace (read it with sffn_read_device_error); the offending element is
+ *    skipped, nothing traps.
+ *  - All device pointers must be 16-byte aligned (128-bit loads) unless stated.
+ *  - Matrices are row-major.  The three weight matrices are stored neuron-major,
+ *    each [d_ff, d_model]: w_gate[j,:], w_up[j,:] and w_downT[j,:] = W_down[:,j].
+ *  - Shape limits: d_model % 8 == 0 (fp32/bf16), d_model % 64 == 0 (int4-g64),
+ *    8 <= d_model <= 8192, 1 <= d_ff <= 65536, 1 <= B <= 8.
+ */
+#ifndef SFFN_H
+#define SFFN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st *sffn_stream_t;
+
+typedef enum {
+    SFFN_OK = 0,
+    SFFN_ERR_INVALID_ARG = 1, /* null pointer, unknown enum value, parameter out of range */
+    SFFN_ERR_SHAPE = 2,       /* dimension out of the supported range                    */
+    SFFN_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned                         */
+    SFFN_ERR_UNSUPPORTED = 4, /* valid but not implemented combination / device           */
+    SFFN_ERR_WORKSPACE = 5,   /* workspace missing, misaligned or smaller than required   */
+    SFFN_ERR_CUDA = 6,        /* a CUDA runtime call or launch failed                     */
+    SFFN_ERR_TIMEOUT = 7,     /* a bounded device-side wait gave up (device error word)   */
+    SFFN_ERR_DEVICE = 8       /* a device-side contract violation was recorded            */
+} sffn_status;
+
+typedef enum { SFFN_MODE_EXACT = 0, SFFN_MODE_THRESHOLD = 1, SFFN_MODE_KEEP_RATIO = 2 } sffn_mode;
+typedef enum { SFFN_ACT_RELU = 0, SFFN_ACT_SILU = 1 } sffn_act;
+/* Weight storage.  INT4_G64: symmetric int4, two's-complement codes packed two
+ * per byte (low nibble = even column), one fp16 scale per 64 consecutive
+ * elements of a stored row; value = code * scale. */
+typedef enum { SFFN_F32 = 0, SFFN_BF16 = 1, SFFN_INT4_G64 = 2 } sffn_wdtype;
+/* Score used by the threshold and keep-ratio modes:
+ *   GATE     score_j = |act(g_j)| * ||W_down[:, j]||_2          (W_up stays sparse)
+ *   GATE_UP  score_j = |act(g_j) * u_j| * ||W_down[:, j]||_2    (needs every u_j,
+ *            so W_up is read in full and only W_down stays sparse). */
+typedef enum { SFFN_SCORE_GATE = 0, SFFN_SCORE_GATE_UP = 1 } sffn_score;
+
+/* One FFN layer.  Host struct holding device pointers. */
+typedef struct {
+    int32_t wdtype;          /* sffn_wdtype                                           */
+    int32_t act;             /* sffn_act                                              */
+    int32_t d_model, d_ff;
+    const void *w_gate;      /* [d_ff, d_model] (int4: uint8 [d_ff, d_model/2])       */
+    const void *w_up;        /* [d_ff, d_model]                                       */
+    const void *w_downT;     /* [d_ff, d_model], row j = column j of W_down           */
+    const void *s_gate;      /* int4 only: fp16 [d_ff, d_model/64]; else NULL         */
+    const void *s_up;        /* int4 only                                             */
+    const void *s_downT;     /* int4 only                                             */
+    const float *b_gate;     /* [d_ff] fp32 gate bias, or NULL                         */
+    const float *down_norms; /* [d_ff] fp32 ||W_down[:, j]||_2 (see sffn_down_norms);
+                                needed by the threshold / keep-ratio modes, else may be NULL */
+} sffn_ffn_weights;
+
+/* Bytes of workspace needed by a call.  which: 0 = sffn_decode (n = B),
+ * 1 = sffn_token_select (n = L), 2 = sffn_prefill (n = L).  Returns 0 for an
+ * invalid request.  The size depends on the device's SM count (current device). */
+size_t sffn_workspace_size(int which, int n, const sffn_ffn_weights *w);
+
+/* norms[j] = ||W_down[:, j]||_2 = sqrt(sum_i w_downT[j, i]^2) of the
+ * (dequantised) weights, fp32 [d_ff].  The weight-aware prior of the WiSparse
+ * write-up, sec. 2.3, with p = 2 on the down projection's column. */
+sffn_status sffn_down_norms(const sffn_ffn_weights *w, float *norms, sffn_stream_t stream);
+
+/* Decode B tokens (1 <= B <= 8) through one layer, skipping inactive neurons.
+ *   x          [B, d_model]: fp32 when wdtype == F32, else bf16.
+ *   mode       sffn_mode; param = tau for THRESHOLD (keep iff score >= tau,
+ *              tau >= 0), keep_ratio in (0, 1] for KEEP_RATIO (keep the
+ *              k = max(1, floor(d_ff * keep_ratio)) largest scores, ties to the
+ *              lower index), ignored for EXACT (keep iff act(g_j) != 0).
+ *   score      sffn_score (threshold / keep-ratio only).
+ *   out        [B, d_model], same dtype as x: sum over the token's active j of
+ *              act(g_j) * u_j * W_down[:, j], fp32 accumulation, rounded once.
+ *   active_idx [B, d_ff] int32: row b holds the token's active neurons in
+ *              ascending order in its first n_active[b] entries (the rest is
+ *              unspecified).  n_active [B] int32.
+ * For B > 1 the W_up / W_down rows of the union of the tokens' active sets are
+ * read once and each token is masked to its own set. */
+sffn_status sffn_decode(const void *x, int B, const sffn_ffn_weights *w, int mode, int score,
+                        float param, void *out, int32_t *active_idx, int32_t *n_active,
+                        void *workspace, size_t ws_bytes, sffn_stream_t stream);
+
+/* Scores of every neuron for B tokens, fp32 [B, d_ff] (score kind as in
+ * sffn_decode; down_norms required).  Reads the gate (and for GATE_UP the up
+ * projection) in full; used to calibrate thresholds offline. */
+sffn_status sffn_gate_scores(const void *x, int B, const sffn_ffn_weights *w, int score,
+                             float *scores, void *workspace, size_t ws_bytes, sffn_stream_t stream);
+
+/* Token selection for a prefill of L tokens (RedKnot selection rules):
+ *   importance s_t = ||y_attn[t, :]||_2 (y_attn bf16 [L, d_model]);
+ *   if mass_thresh >= 1 or sum_t s_t == 0: every token;
+ *   else the shortest prefix of the tokens ordered by (s desc, t asc) whose
+ *   importance sum reaches mass_thresh * sum_t s_t (the crossing token is
+ *   included; none if mass_thresh <= 0), united with the last recent_n tokens,
+ *   then extended in the same order up to min(min_keep, L) tokens.
+ * Writes sel_idx[0 .. n_sel) ascending (int32 [L]) and n_sel (int32 [1]).
+ * recent_n >= 0, min_keep >= 1, 1 <= L <= 1048576, d_model % 8 == 0. */
+sffn_status sffn_token_select(const void *y_attn, int L, int d_model, float mass_thresh,
+                              int recent_n, int min_keep, int32_t *sel_idx, int32_t *n_sel,
+                              void *workspace, size_t ws_bytes, sffn_stream_t stream);
+
+/* Token-selective prefill (RedKnot Algorithm 1): Y = bf16(x + y_attn) for every
+ * row; for the selected rows out[t] = bf16(Y[t] + FFN(Y[t])) with
+ * FFN(y) = W_down . (SiLU(W_gate . y) (.) (W_up . y)); for the others
+ * out[t] = Y[t] (Z = 0).  x, y_attn, out: bf16 [L, d_model].  sel_idx / n_sel as
+ * written by sffn_token_select (ascending, device).  Weights: bf16, act SILU,
+ * no gate bias, d_model % 64 == 0, d_ff % 128 == 0. */
+sffn_status sffn_prefill(const void *x, const void *y_attn, int L, const sffn_ffn_weights *w,
+                         const int32_t *sel_idx, const int32_t *n_sel, void *out, void *workspace,
+                         size_t ws_bytes, sffn_stream_t stream);
+
+/* Copy the workspace's device error word to *code (host) and clear it; waits
+ * for `stream`.  0 = no error; otherwise an sffn_status value. */
+sffn_status sffn_read_device_error(void *workspace, int32_t *code, sffn_stream_t stream);
+
+/* Static description of a status code. */
+const char *sffn_status_string(sffn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SFFN_H */

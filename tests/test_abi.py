@@ -1,0 +1,127 @@
+"""The C-ABI boundary: the library loads and exports every symbol the header
+declares (CPU), host-side argument checks return the documented status before
+anything is launched (CPU where no CUDA call is reached, GPU otherwise)."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sffn.h")
+
+
+@pytest.fixture(scope="module")
+def S():
+    from activation_sparse_ffn_gemv_gb300 import build as B
+    B.build()
+    from activation_sparse_ffn_gemv_gb300 import sffn
+    sffn.lib()
+    return sffn
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(sffn_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for must in ("sffn_decode", "sffn_token_select", "sffn_prefill", "sffn_workspace_size",
+                 "sffn_status_string", "sffn_down_norms", "sffn_read_device_error"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(S):
+    lib = C.CDLL(S.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(S):
+    for st in range(9):
+        assert S.status_string(st) and S.status_string(st) != "unknown status"
+    assert S.status_string(99) == "unknown status"
+
+
+def test_null_arguments_rejected_before_any_cuda_call(S):
+    L = S.lib()
+    w = S.FFNWeights(S.BF16, S.ACT_RELU, 64, 128, 16, 16, 16, None, None, None, None, None)
+    # x == NULL
+    assert L.sffn_decode(None, 1, C.byref(w), 0, 0, 0.0, 16, 16, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+    # unknown mode / score
+    assert L.sffn_decode(16, 1, C.byref(w), 7, 0, 0.0, 16, 16, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+    assert L.sffn_decode(16, 1, C.byref(w), 0, 5, 0.0, 16, 16, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+    # weights struct missing
+    assert L.sffn_decode(16, 1, None, 0, 0, 0.0, 16, 16, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+    # token select / prefill null pointers
+    assert L.sffn_token_select(None, 16, 64, 0.5, 4, 1, 16, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+    assert L.sffn_prefill(None, 16, 16, C.byref(w), 16, 16, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+    assert L.sffn_down_norms(None, 16, None) == S.ERR_INVALID_ARG
+
+
+def test_shape_and_parameter_checks_before_any_cuda_call(S):
+    L = S.lib()
+
+    def wts(**kw):
+        f = dict(wdtype=S.BF16, act=S.ACT_RELU, d_model=64, d_ff=128)
+        f.update(kw)
+        return S.FFNWeights(f["wdtype"], f["act"], f["d_model"], f["d_ff"], 16, 16, 16, 16, 16, 16, None, 16)
+
+    def dec(w, B=1, mode=0, param=0.0, x=16):
+        return L.sffn_decode(x, B, C.byref(w), mode, 0, param, 16, 16, 16, 256, 1 << 20, None)
+
+    assert dec(wts(d_model=12)) == S.ERR_SHAPE                 # d % 8
+    assert dec(wts(d_model=96, wdtype=S.INT4_G64)) == S.ERR_SHAPE  # int4 needs d % 64
+    assert dec(wts(d_ff=0)) == S.ERR_SHAPE
+    assert dec(wts(), B=0) == S.ERR_SHAPE
+    assert dec(wts(), B=9) == S.ERR_SHAPE
+    assert dec(wts(d_model=8192)) == S.ERR_SHAPE               # decode limit 4096
+    assert dec(wts(), x=8) == S.ERR_ALIGNMENT
+    assert dec(wts(), mode=2, param=0.0) == S.ERR_INVALID_ARG  # keep ratio in (0, 1]
+    assert dec(wts(), mode=2, param=1.5) == S.ERR_INVALID_ARG
+    assert dec(wts(), mode=1, param=-1.0) == S.ERR_INVALID_ARG # tau >= 0
+    assert dec(wts(act=5)) == S.ERR_INVALID_ARG
+    assert L.sffn_token_select(16, 0, 64, 0.5, 4, 1, 16, 16, 256, 1 << 20, None) == S.ERR_SHAPE
+    assert L.sffn_token_select(16, 16, 64, 0.5, -1, 1, 16, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+    assert L.sffn_token_select(16, 16, 64, 0.5, 4, 0, 16, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+    assert L.sffn_token_select(8, 16, 64, 0.5, 4, 1, 16, 16, 256, 1 << 20, None) == S.ERR_ALIGNMENT
+    w = wts(act=S.ACT_SILU)
+    assert L.sffn_prefill(16, 16, 16, C.byref(wts()), 16, 16, 16, 256, 1 << 20, None) == S.ERR_UNSUPPORTED  # ReLU
+    assert L.sffn_prefill(16, 16, 0, C.byref(w), 16, 16, 16, 256, 1 << 20, None) == S.ERR_SHAPE
+    assert L.sffn_workspace_size(5, 1, None) == 0
+
+
+@pytest.mark.gpu
+def test_workspace_checks_on_gpu(S):
+    from activation_sparse_ffn_gemv_gb300 import workloads as W
+    layer = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in
+             W.make_ffn_layer(2, seed=1, d_model=64, d_ff=128).items()}
+    w = S.Weights(layer)
+    x = W.make_tokens(2, 1, d_model=64).cuda()
+    need = S.workspace_size(S.WS_DECODE, 1, w)
+    assert need > 0
+    ws = torch.zeros(need + 512, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(x)
+    idx = torch.empty((1, 128), dtype=torch.int32, device="cuda")
+    n = torch.empty(1, dtype=torch.int32, device="cuda")
+    L = S.lib()
+    st = L.sffn_decode(x.data_ptr(), 1, w.ref(), 0, 0, 0.0, out.data_ptr(), idx.data_ptr(), n.data_ptr(),
+                       ws.data_ptr(), need - 1, None)
+    assert st == S.ERR_WORKSPACE
+    st = L.sffn_decode(x.data_ptr(), 1, w.ref(), 0, 0, 0.0, out.data_ptr(), idx.data_ptr(), n.data_ptr(),
+                       ws.data_ptr() + 16, need, None)
+    assert st == S.ERR_WORKSPACE           # not 256-byte aligned
+    # threshold mode without down_norms
+    st = L.sffn_decode(x.data_ptr(), 1, w.ref(), 1, 0, 0.5, out.data_ptr(), idx.data_ptr(), n.data_ptr(),
+                       ws.data_ptr(), need, None)
+    assert st == S.ERR_INVALID_ARG
+    st = L.sffn_decode(x.data_ptr(), 1, w.ref(), 0, 0, 0.0, out.data_ptr(), idx.data_ptr(), n.data_ptr(),
+                       ws.data_ptr(), need, None)
+    assert st == S.OK
+    torch.cuda.synchronize()
+    assert S.read_device_error(ws) == 0

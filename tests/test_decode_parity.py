@@ -1,0 +1,134 @@
+"""GPU parity of sffn_decode against the fp64 oracle (sets within the tie band,
+outputs within the per-token relative L2 bound), through the C ABI."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from activation_sparse_ffn_gemv_gb300 import workloads as W
+from tests.parity import run_and_check_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sffn():
+    from activation_sparse_ffn_gemv_gb300 import sffn as S
+    S.lib()
+    return S
+
+
+def _cfg(base, **kw):
+    c = dict(W.CONFIGS[base])
+    c.update(kw)
+    return c
+
+
+# small shapes: several gate chunks, ragged tails (d not a multiple of 256, F not
+# a multiple of the chunk), both weight dtypes, 1..8 tokens
+SMALL = [
+    # (cfg, d, F, wdtype, act, B)
+    (1, 256, 688, "f32", "relu", 1),
+    (1, 136, 1001, "f32", "relu", 3),
+    (2, 520, 1333, "bf16", "relu", 1),
+    (2, 264, 777, "bf16", "relu", 2),
+    (2, 1024, 2050, "bf16", "relu", 5),
+    (2, 4096, 300, "bf16", "relu", 8),
+    (2, 8, 33, "bf16", "relu", 1),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: "-".join(map(str, c)))
+def test_exact_gating_small(sffn, case):
+    cfg, d, F, wd, act, B = case
+    layer = W.make_ffn_layer(cfg, seed=7, d_model=d, d_ff=F, wdtype=wd, act=act)
+    x = W.make_tokens(cfg, B, seed=3, d_model=d, xdtype="f32" if wd == "f32" else "bf16")
+    r = run_and_check_decode(sffn, layer, x, "exact")
+    assert (r["n_active"] > 0).all()
+
+
+@pytest.mark.parametrize("score", ["gate", "gate_up"])
+@pytest.mark.parametrize("B", [1, 4])
+def test_threshold_small(sffn, score, B):
+    d, F = 512, 1536
+    layer = W.make_ffn_layer(3, seed=11, d_model=d, d_ff=F)
+    x = W.make_tokens(3, B, seed=5, d_model=d)
+    # tau at a mid quantile of the oracle's own scores so the set is non-trivial
+    from tests.oracle_io import ffn_from_layer, mat_from_act
+    import oracle as O
+    ref = O.decode(ffn_from_layer(layer), mat_from_act(x), O.THRESHOLD,
+                   O.SCORE_GATE if score == "gate" else O.SCORE_GATE_UP, 0.0, details=True)
+    tau = float(np.quantile(ref["score"], 0.7))
+    r = run_and_check_decode(sffn, layer, x, "threshold", score, tau)
+    frac = r["n_active"].mean() / F
+    assert 0.2 < frac < 0.4
+
+
+@pytest.mark.parametrize("score", ["gate", "gate_up"])
+@pytest.mark.parametrize("ratio", [1.0, 0.5, 0.25, 0.125, 1e-6])
+def test_keep_ratio_small(sffn, score, ratio):
+    d, F = 384, 1100
+    layer = W.make_ffn_layer(3, seed=13, d_model=d, d_ff=F)
+    x = W.make_tokens(3, 2, seed=6, d_model=d)
+    run_and_check_decode(sffn, layer, x, "keep_ratio", score, ratio)
+
+
+def test_keep_ratio_batch_union(sffn):
+    d, F = 256, 700
+    layer = W.make_ffn_layer(3, seed=17, d_model=d, d_ff=F)
+    x = W.make_tokens(3, 7, seed=8, d_model=d)
+    run_and_check_decode(sffn, layer, x, "keep_ratio", "gate", 0.3)
+
+
+def test_threshold_zero_is_dense(sffn):
+    d, F = 256, 640
+    layer = W.make_ffn_layer(3, seed=19, d_model=d, d_ff=F)
+    x = W.make_tokens(3, 3, seed=9, d_model=d)
+    r = run_and_check_decode(sffn, layer, x, "threshold", "gate", 0.0)
+    assert (r["n_active"] == F).all()
+
+
+def test_no_active_neuron_gives_zero(sffn):
+    d, F = 64, 100
+    layer = W.make_ffn_layer(2, seed=23, d_model=d, d_ff=F)
+    layer["b_gate"] = torch.full((F,), -1e4)
+    x = W.make_tokens(2, 2, seed=1, d_model=d)
+    r = run_and_check_decode(sffn, layer, x, "exact")
+    assert (r["n_active"] == 0).all()
+    assert not torch.any(r["out"].float() != 0)
+
+
+def test_ties_keep_lower_index(sffn):
+    # duplicated neurons have bit-identical scores; keep-ratio must take the lower index
+    d, F = 64, 64
+    layer = W.make_ffn_layer(3, seed=29, d_model=d, d_ff=F)
+    for name in ("w_gate", "w_up", "w_downT"):
+        layer[name][32:] = layer[name][:32]
+    x = W.make_tokens(3, 1, seed=2, d_model=d)
+    r = run_and_check_decode(sffn, layer, x, "keep_ratio", "gate", 0.25)
+    assert r["exempt"] == 0
+
+
+# full configuration shapes (a few tokens; the oracle computes them one by one)
+
+def test_config_tiny_reglu_full(sffn):
+    layer = W.make_ffn_layer(1, seed=0)
+    x = W.make_tokens(1, 64, seed=0)
+    r = run_and_check_decode(sffn, layer, x, "exact", batch=1)
+    assert abs(r["n_active"].mean() / layer["d_ff"] - 0.1587) < 0.01
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_config_llama_reglu_full(sffn, B):
+    layer = W.make_ffn_layer(2, seed=0)
+    x = W.make_tokens(2, B, seed=B)
+    r = run_and_check_decode(sffn, layer, x, "exact", nthreads=16)
+    assert abs(r["n_active"].mean() / layer["d_ff"] - 0.125) < 0.02
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8])
+def test_config_qwen_keep_ratio_full(sffn, M):
+    layer = W.make_ffn_layer(3, seed=0, layer=M)
+    x = W.make_tokens(3, 1, seed=M)
+    run_and_check_decode(sffn, layer, x, "keep_ratio", "gate_up", 1.0 / M, nthreads=16)
