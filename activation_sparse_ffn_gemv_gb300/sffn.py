@@ -23,6 +23,7 @@ ACT_RELU, ACT_SILU = 0, 1
 F32, BF16, INT4_G64 = 0, 1, 2
 SCORE_GATE, SCORE_GATE_UP = 0, 1
 WS_DECODE, WS_SELECT, WS_PREFILL = 0, 1, 2
+NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _WDTYPE = {"f32": F32, "bf16": BF16, "int4_g64": INT4_G64}
 _ACT = {"relu": ACT_RELU, "silu": ACT_SILU}
@@ -66,6 +67,8 @@ def lib():
         L.sffn_token_select.restype = I
         L.sffn_prefill.argtypes = [P, P, I, W, P, P, P, P, S, P]
         L.sffn_prefill.restype = I
+        L.sffn_decode_noalloc.argtypes = [P, I, W, I, I, F, P, P, P, P]
+        L.sffn_decode_noalloc.restype = I
         L.sffn_read_device_error.argtypes = [P, C.POINTER(C.c_int32), P]
         L.sffn_read_device_error.restype = I
         _lib = L
@@ -153,6 +156,24 @@ def decode(x: torch.Tensor, w: Weights, mode: int, score: int = SCORE_GATE, para
                            _ptr(active_idx), _ptr(n_active), _ptr(workspace), workspace.numel(),
                            _stream(stream))
     _check(st, "sffn_decode")
+    return out, active_idx, n_active
+
+
+def decode_noalloc(x: torch.Tensor, w: Weights, mode: int, score: int = SCORE_GATE, param: float = 0.0,
+                   out=None, active_idx=None, n_active=None, stream=None):
+    """sffn_decode with the library's built-in scratch array instead of a
+    caller workspace, for callers that cannot allocate device memory (limit:
+    NOALLOC_SCRATCH_BYTES of workspace; calls must not overlap on the GPU)."""
+    B = x.shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    if active_idx is None:
+        active_idx = torch.empty((B, w.d_ff), dtype=torch.int32, device=x.device)
+    if n_active is None:
+        n_active = torch.empty(B, dtype=torch.int32, device=x.device)
+    st = lib().sffn_decode_noalloc(_ptr(x), B, w.ref(), int(mode), int(score), float(param), _ptr(out),
+                                   _ptr(active_idx), _ptr(n_active), _stream(stream))
+    _check(st, "sffn_decode_noalloc")
     return out, active_idx, n_active
 
 

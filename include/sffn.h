@@ -127,6 +127,36 @@ sffn_status sffn_decode(const void *x, int B, const sffn_ffn_weights *w, int mod
                         float param, void *out, int32_t *active_idx, int32_t *n_active,
                         void *workspace, size_t ws_bytes, sffn_stream_t stream);
 
+/* Size of the scratch array built into the library for sffn_decode_noalloc. */
+#define SFFN_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/* sffn_decode without a workspace argument.  No page describes this call: it
+ * exists for callers that cannot allocate device memory themselves -- code that
+ * is handed its input and output buffers by a host framework or plugin
+ * interface and has no device allocator of its own, or that must not allocate
+ * once it is running (a latency-critical serving loop with a fixed memory
+ * budget).  Such callers cannot provide the `workspace` that sffn_decode takes.
+ *
+ * Instead the scratch memory comes from one fixed array of
+ * SFFN_NOALLOC_SCRATCH_BYTES (4 MiB) compiled into the library; every GPU that
+ * loads the library holds that array until the process exits.  Arguments and
+ * results are exactly those of sffn_decode.  The call allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *  - A request whose workspace (sffn_workspace_size(0, B, w)) would exceed the
+ *    array is rejected with SFFN_ERR_WORKSPACE before anything is launched.
+ *    On a 152-SM GB300 that admits B = 1 at d_model 4096 / d_ff 11008 and
+ *    B <= 2 at d_model 2048 / d_ff 11008.
+ *  - The first call on each device looks up the array's device address (with
+ *    that device current); make that first call before any stream capture.
+ *  - All calls share the one array, which keeps the previous call's contents
+ *    (every word is written before it is read; the device error word is
+ *    cleared at the start of each call).  Calls that can overlap on the GPU
+ *    (different streams, different host threads) race on it: issue them in
+ *    one stream order. */
+sffn_status sffn_decode_noalloc(const void *x, int B, const sffn_ffn_weights *w, int mode, int score,
+                                float param, void *out, int32_t *active_idx, int32_t *n_active,
+                                sffn_stream_t stream);
+
 /* Scores of every neuron for B tokens, fp32 [B, d_ff] (score kind as in
  * sffn_decode; down_norms required).  Reads the gate (and for GATE_UP the up
  * projection) in full; used to calibrate thresholds offline. */
