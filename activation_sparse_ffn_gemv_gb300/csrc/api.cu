@@ -11,6 +11,7 @@ namespace sffn {
 namespace {
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];
+int g_smem_optin[kMaxDevices];
 std::mutex g_mu;
 
 struct SmemEntry {
@@ -32,6 +33,18 @@ int device_sm_count() {
         g_sm_count[dev] = n;
     }
     return g_sm_count[dev];
+}
+
+int device_smem_optin() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_smem_optin[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+        g_smem_optin[dev] = n;
+    }
+    return g_smem_optin[dev];
 }
 
 cudaError_t set_max_smem(const void *kernel, int bytes) {

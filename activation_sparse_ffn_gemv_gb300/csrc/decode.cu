@@ -54,6 +54,60 @@ struct WBF16 {
     }
 };
 
+// Copy the activations x [nb, d] into shared memory in their own dtype
+// [NBpad, d] (rows >= nb zero), 128-bit units, four loads in flight per thread.
+template <class W>
+SFFN_DEV void stage_x_raw(void *xs, const void *x, int nb, int NBpad, int d) {
+    constexpr int XE = 16 / (int)sizeof(typename W::X);
+    const int per_row = d / XE;
+    const int total = NBpad * per_row;
+    uint4 *dst = static_cast<uint4 *>(xs);
+    for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int u = base + k * blockDim.x;
+            v[k] = (u < total && u / per_row < nb) ? ldg_v4(static_cast<const char *>(x) + (size_t)u * 16)
+                                                   : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int u = base + k * blockDim.x;
+            if (u < total) dst[u] = v[k];
+        }
+    }
+}
+
+// Stage the activations x [nb, d] into shared memory as fp32 [NBpad, d]
+// (rows >= nb zero).  128-bit loads, four in flight per thread, so staging
+// costs one memory round trip instead of one per element.
+template <class W>
+SFFN_DEV void stage_x(float *xs, const void *x, int nb, int NBpad, int d) {
+    constexpr int XE = 16 / (int)sizeof(typename W::X);  // elements per 16-byte unit of x
+    const int per_row = d / XE;
+    const int total = NBpad * per_row;
+    for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
+        uint4 v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int u = base + k * blockDim.x;
+            v[k] = (u < total && u / per_row < nb) ? ldg_v4(static_cast<const char *>(x) + (size_t)u * 16)
+                                                   : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int u = base + k * blockDim.x;
+            if (u < total) {
+                float f[XE];
+                W::unpack(v[k], f);
+                float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)u * XE);
+#pragma unroll
+                for (int q = 0; q < XE / 4; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // down-projection column norms: norms[j] = ||W_downT[j, :]||_2
 // ---------------------------------------------------------------------------
@@ -80,6 +134,16 @@ __global__ void __launch_bounds__(256) k_down_norms(const void *wdT, int d, int 
 // ---------------------------------------------------------------------------
 // gate kernel
 // ---------------------------------------------------------------------------
+//
+// One CTA per SM owns R consecutive neurons (a "chunk").  Lane 0 of warp 0
+// streams the chunk's gate rows (and, for the gate-and-up score, the up rows)
+// into a ring of shared-memory stages with 1-D bulk copies (TMA) completing on
+// mbarriers; eight consumer warps take one row each, form the dot products
+// from shared memory, apply bias / act / score and decide.  For the exact and
+// threshold rules a warp whose row is active for some token immediately reads
+// that neuron's W_up row and forms u_j and h_j = a_j * u_j, so the down kernel
+// needs nothing but (j, h_j).  Every mbarrier wait is time-bounded; on a timeout
+// the CTA records SFFN_ERR_TIMEOUT, drains its own copies and stops.
 
 struct GateArgs {
     const void *wg, *wu;
@@ -88,132 +152,319 @@ struct GateArgs {
     int d, F, nb, R, C;
     int act, mode, score_kind;
     float tau;
-    int decide;           // 1: exact / threshold decision + lists here
-    float *aeff;          // [nb, F] act value, zeroed where the token is inactive (if decide)
-    float *uval;          // [nb, F] u_j (UP only)
+    int decide;           // 1: exact / threshold decision, lists and h here
+    int list_u;           // list whose entries carry h values (0 if nb == 1, else the union)
+    int stages;           // rows in flight per warp (its ring stages)
+    float *aeff;          // !decide: [nb, F] raw act values (or null)
+    float *uval;          // !decide, UP: [nb, F] u_j (or null)
     float *score;         // [nb, F] or null
-    int *cnt, *lidx;      // chunk counts / chunk-local lists (if decide)
+    int *cnt, *lidx;      // decide: chunk counts / chunk-local ascending lists
+    float *lh;            // decide: [nb, F] h values aligned with list list_u (unfused only)
+    int32_t *err;
+    const void *wdT;      // decide: down projection, read for this chunk's active rows
+    float *part;          // decide: [C, nb, d] this CTA's fp32 partial of the output
 };
 
-constexpr int kGateThreads = 256;
-constexpr int kMaxChunk = kGateThreads;  // R <= blockDim so one scan pass compacts a chunk
+constexpr int kGateWarps = 8;           // each warp streams its own rows
+constexpr int kGateThreads = 32 * kGateWarps;
+constexpr int kMaxChunk = 256;  // R <= kMaxChunk <= blockDim: one scan pass compacts a chunk
 
 template <class W, int NB, bool UP>
-__global__ void __launch_bounds__(kGateThreads) k_gate(GateArgs a) {
-    extern __shared__ float xs[];  // [NB][d] fp32 (tokens >= nb are zero)
-    __shared__ uint8_t sflag[kMaxChunk];
-    __shared__ int scan_tmp[34];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+__global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
+    extern __shared__ __align__(128) unsigned char smraw[];
     const int d = a.d, F = a.F;
-    // x is a call input, complete before this call's first kernel started.
-    for (int i = tid; i < NB * d; i += blockDim.x) {
-        const int b = i / d;
-        xs[i] = b < a.nb ? W::load_x(a.x, (size_t)b * d + (i - b * d)) : 0.f;
-    }
+    const uint32_t units = (uint32_t)(d / W::E);  // 16-byte units per row
+    const uint32_t row_bytes = units * 16u;
+    const uint32_t stage_bytes = UP ? 2u * row_bytes : row_bytes;
+    const int D = a.stages;                        // stages (rows in flight) per warp
+    unsigned char *ring = smraw;                   // [warps][D] stages
+    unsigned char *xraw = smraw + (size_t)kGateWarps * D * stage_bytes;
+    const uint4 *xs = reinterpret_cast<const uint4 *>(xraw);   // x in its own dtype [NB][d]
+    uint64_t *full = reinterpret_cast<uint64_t *>(xraw + (size_t)NB * row_bytes);  // [warps][D]
+    uint64_t *dbar = full + (size_t)kGateWarps * D;  // active-row copies after the stream
+    __shared__ uint8_t sflag[kMaxChunk];
+    __shared__ float sh[kMaxChunk][NB];
+    __shared__ float sbias[kMaxChunk], snorm[kMaxChunk];
+    __shared__ int scan_tmp[34];
+    __shared__ volatile int s_abort;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row0 = blockIdx.x * a.R;
     const int nrows = min(a.R, F - row0);
-    __syncthreads();
+    // warp w handles rows w, w + 8, w + 16, ... of the chunk
+    const int nmine = nrows > warp ? (nrows - warp + kGateWarps - 1) / kGateWarps : 0;
+    uint64_t *wfull = full + (size_t)warp * D;
+    unsigned char *wring = ring + (size_t)warp * D * stage_bytes;
+    const char *gbase = static_cast<const char *>(a.wg) + (size_t)row0 * row_bytes;
+    const char *ubase = UP ? static_cast<const char *>(a.wu) + (size_t)row0 * row_bytes : nullptr;
+    uint64_t pol = 0;
+    // Each warp keeps its own D row copies in flight (1-D bulk copies issued by
+    // its lane 0) and re-issues into a stage as soon as it has consumed it: no
+    // producer warp, so a slow warp never holds back another warp's stream.
+    // Weights are constant inputs: they stream before the dependency wait.
+    if (lane == 0) {
+        for (int i = 0; i < D; ++i) mbar_init(&wfull[i], 1);
+        mbar_fence_init();
+        pol = l2_evict_first_policy();
+        for (int i = 0; i < D && i < nmine; ++i) {
+            const size_t r = (size_t)(warp + i * kGateWarps);
+            mbar_arrive_expect_tx(&wfull[i], stage_bytes);
+            bulk_load(wring + (size_t)i * stage_bytes, gbase + r * row_bytes, row_bytes, &wfull[i], pol);
+            if (UP) bulk_load(wring + (size_t)i * stage_bytes + row_bytes, ubase + r * row_bytes, row_bytes, &wfull[i], pol);
+        }
+    }
+    if (tid == 0) {
+        s_abort = 0;
+        mbar_init(dbar, 1);
+        mbar_fence_init();
+    }
+    // x may be the previous layer's output: read it only after the dependency wait
     griddep_wait();
-    griddep_launch_dependents();
-
-    const int units = d / W::E;  // 16-byte units per row
-    const size_t row_bytes = (size_t)units * 16;
-    constexpr int BLK = UP ? 8 : 16;  // units in flight per lane per row stream
-
-    for (int r = warp; r < nrows; r += nwarps) {
-        const int j = row0 + r;
-        const char *pg = static_cast<const char *>(a.wg) + (size_t)j * row_bytes;
-        const char *pu = UP ? static_cast<const char *>(a.wu) + (size_t)j * row_bytes : nullptr;
-        float accg[NB], accu[NB];
+    {
+        constexpr int XE = 16 / (int)sizeof(typename W::X);
+        const int per_row = d / XE, total = NB * per_row;
+        uint4 *dst = reinterpret_cast<uint4 *>(xraw);
+        for (int u = tid; u < total; u += blockDim.x)
+            dst[u] = u / per_row < a.nb ? ldg_v4(static_cast<const char *>(a.x) + (size_t)u * 16)
+                                        : make_uint4(0, 0, 0, 0);
+        for (int i = tid; i < nrows; i += blockDim.x) {
+            sbias[i] = a.bias ? a.bias[row0 + i] : 0.f;
+            snorm[i] = a.norms ? a.norms[row0 + i] : 0.f;
+        }
+    }
+    __syncthreads();
+    {
+        // This lane always handles units lane, lane + 32, ... of a row: for one
+        // token its slice of x is unpacked into registers once and reused for
+        // every row.  Units per lane <= UPL (d_model <= 4096).
+        constexpr int UPL = W::E == 8 ? 16 : 32;
+        constexpr bool XREG = NB == 1;
+        float xr[XREG ? UPL * W::E : 1];
+        if (XREG) {
 #pragma unroll
-        for (int b = 0; b < NB; ++b) accg[b] = accu[b] = 0.f;
-        for (int u0 = 0; u0 < units; u0 += 32 * BLK) {
-            uint4 vg[BLK], vu[UP ? BLK : 1];
+            for (int i = 0; i < UPL; ++i) {
+                const uint32_t u = i * 32 + lane;
+                float f[W::E];
+                W::unpack(u < units ? xs[u] : make_uint4(0, 0, 0, 0), f);
 #pragma unroll
-            for (int i = 0; i < BLK; ++i) {
-                const int u = u0 + i * 32 + lane;
-                if (u < units) {
-                    vg[i] = ldg_stream(pg + (size_t)u * 16);
-                    if (UP) vu[i] = ldg_stream(pu + (size_t)u * 16);
-                }
+                for (int e = 0; e < W::E; ++e) xr[(XREG ? i * W::E + e : 0)] = f[e];
             }
+        }
+        for (int k = 0; k < nmine; ++k) {
+            const int si = k % D;
+            const bool ok = mbar_wait(&wfull[si], (uint32_t)(k / D) & 1u);
+            if (!__all_sync(0xffffffffu, ok && !s_abort)) {
+                // a wait timed out here or in another warp: record it, let this
+                // warp's own copies in flight land (bounded), then stop
+                if (lane == 0) {
+                    if (!ok) {
+                        s_abort = 1;
+                        record_error(a.err, SFFN_ERR_TIMEOUT);
+                    }
+                    for (int kk = k; kk < min(nmine, k + D); ++kk) mbar_wait(&wfull[kk % D], (uint32_t)(kk / D) & 1u);
+                }
+                __syncwarp();
+                break;
+            }
+            {
+                const int r = warp + k * kGateWarps;
+                const unsigned char *st = wring + (size_t)si * stage_bytes;
+                // 4 independent accumulators per token and projection (ILP)
+                float accg[NB][4], accu[NB][4];
 #pragma unroll
-            for (int i = 0; i < BLK; ++i) {
-                const int u = u0 + i * 32 + lane;
-                if (u < units) {
-                    float fg[W::E];
-                    W::unpack(vg[i], fg);
-                    float fu[W::E];
-                    if (UP) W::unpack(vu[UP ? i : 0], fu);
+                for (int b = 0; b < NB; ++b)
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        const float4 *xp = reinterpret_cast<const float4 *>(xs + b * d + u * W::E);
+                    for (int c = 0; c < 4; ++c) accg[b][c] = accu[b][c] = 0.f;
 #pragma unroll
-                        for (int q = 0; q < W::E / 4; ++q) {
-                            const float4 xv = xp[q];
-                            accg[b] = fmaf(fg[4 * q + 0], xv.x, accg[b]);
-                            accg[b] = fmaf(fg[4 * q + 1], xv.y, accg[b]);
-                            accg[b] = fmaf(fg[4 * q + 2], xv.z, accg[b]);
-                            accg[b] = fmaf(fg[4 * q + 3], xv.w, accg[b]);
-                            if (UP) {
-                                accu[b] = fmaf(fu[4 * q + 0], xv.x, accu[b]);
-                                accu[b] = fmaf(fu[4 * q + 1], xv.y, accu[b]);
-                                accu[b] = fmaf(fu[4 * q + 2], xv.z, accu[b]);
-                                accu[b] = fmaf(fu[4 * q + 3], xv.w, accu[b]);
+                for (int i0 = 0; i0 < UPL; i0 += 4) {
+                    uint4 vg[4], vu[4];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t u = (i0 + c) * 32 + lane;
+                        vg[c] = u < units ? *reinterpret_cast<const uint4 *>(st + u * 16) : make_uint4(0, 0, 0, 0);
+                        if (UP)
+                            vu[c] = u < units ? *reinterpret_cast<const uint4 *>(st + row_bytes + u * 16)
+                                              : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t u = (i0 + c) * 32 + lane;
+                        float fg[W::E], fu[W::E];
+                        W::unpack(vg[c], fg);
+                        if (UP) W::unpack(vu[c], fu);
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) {
+                            float xf[W::E];
+                            if (XREG) {
+#pragma unroll
+                                for (int e = 0; e < W::E; ++e) xf[e] = xr[XREG ? (i0 + c) * W::E + e : 0];
+                            } else {
+                                W::unpack(u < units ? xs[(size_t)b * units + u] : make_uint4(0, 0, 0, 0), xf);
+                            }
+#pragma unroll
+                            for (int e = 0; e < W::E; ++e) {
+                                accg[b][c] = fmaf(fg[e], xf[e], accg[b][c]);
+                                if (UP) accu[b][c] = fmaf(fu[e], xf[e], accu[b][c]);
                             }
                         }
                     }
+                    if ((i0 + 4) * 32 >= (int)units) break;
                 }
-            }
-        }
-        // every lane gets the full sums; lane b then finishes token b
-        float g = 0.f, uu = 0.f;
+                // stage consumed: refill it with this warp's row k + D
+                __syncwarp();
+                if (lane == 0 && k + D < nmine) {
+                    fence_proxy_async_smem();
+                    const size_t rn = (size_t)(warp + (k + D) * kGateWarps);
+                    mbar_arrive_expect_tx(&wfull[si], stage_bytes);
+                    bulk_load(wring + (size_t)si * stage_bytes, gbase + rn * row_bytes, row_bytes, &wfull[si], pol);
+                    if (UP) bulk_load(wring + (size_t)si * stage_bytes + row_bytes, ubase + rn * row_bytes, row_bytes,
+                                      &wfull[si], pol);
+                }
+                float g = 0.f, uu = 0.f;
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const float sg = warp_sum(accg[b]);
-            const float su = UP ? warp_sum(accu[b]) : 0.f;
-            if (lane == b) { g = sg; uu = su; }
-        }
-        bool active = false;
-        if (lane < a.nb) {
-            if (a.bias) g += a.bias[j];
-            const float av = act_fn(a.act, g);
-            float sc = 0.f;
-            if (a.score) {
-                const float n = a.norms[j];
-                sc = (a.score_kind == SFFN_SCORE_GATE_UP ? fabsf(av * uu) : fabsf(av)) * n;
-                a.score[(size_t)lane * F + j] = sc;
-            }
-            if (a.decide) {
-                if (a.mode == SFFN_MODE_EXACT) {
-                    active = av != 0.f;
-                } else {
-                    const float n = a.norms[j];
-                    const float s = (a.score_kind == SFFN_SCORE_GATE_UP ? fabsf(av * uu) : fabsf(av)) * n;
-                    active = s >= a.tau;
+                for (int b = 0; b < NB; ++b) {
+                    const float sg = warp_sum((accg[b][0] + accg[b][1]) + (accg[b][2] + accg[b][3]));
+                    const float su = UP ? warp_sum((accu[b][0] + accu[b][1]) + (accu[b][2] + accu[b][3])) : 0.f;
+                    if (lane == b) { g = sg; uu = su; }
                 }
-                a.aeff[(size_t)lane * F + j] = active ? av : 0.f;
-            } else if (a.aeff) {
-                a.aeff[(size_t)lane * F + j] = av;
+                const int j = row0 + r;
+                bool active = false;
+                float av = 0.f;
+                if (lane < a.nb) {
+                    g += sbias[r];
+                    av = act_fn(a.act, g);
+                    float sc = 0.f;
+                    if (a.score || (a.decide && a.mode != SFFN_MODE_EXACT)) {
+                        sc = (a.score_kind == SFFN_SCORE_GATE_UP ? fabsf(av * uu) : fabsf(av)) * snorm[r];
+                        if (a.score) a.score[(size_t)lane * F + j] = sc;
+                    }
+                    if (a.decide) {
+                        active = a.mode == SFFN_MODE_EXACT ? av != 0.f : sc >= a.tau;
+                    } else {
+                        if (a.aeff) a.aeff[(size_t)lane * F + j] = av;
+                        if (UP && a.uval) a.uval[(size_t)lane * F + j] = uu;
+                    }
+                }
+                if (!a.decide) continue;
+                const unsigned m = __ballot_sync(0xffffffffu, active) & 0xffu;
+                if (m != 0u && lane == 0) {
+                    bulk_prefetch_l2(static_cast<const char *>(a.wdT) + (size_t)j * row_bytes, row_bytes);
+                    if (!UP) bulk_prefetch_l2(static_cast<const char *>(a.wu) + (size_t)j * row_bytes, row_bytes);
+                }
+                // UP: h_j = a_j u_j now; otherwise the masked a_j, multiplied by u_j later
+                if (lane < NB) sh[r][lane] = active ? (UP ? av * uu : av) : 0.f;
+                if (lane == 0) sflag[r] = (uint8_t)m;
             }
-            if (UP && a.uval) a.uval[(size_t)lane * F + j] = uu;
         }
-        const unsigned m = __ballot_sync(0xffffffffu, active);
-        if (lane == 0) sflag[r] = (uint8_t)(m & 0xffu);
     }
-    if (!a.decide) return;
     __syncthreads();
+    if (!a.decide || s_abort) return;
 
-    // ordered compaction of this chunk, one list per token (+ the union)
-    const int nlists = a.nb + (a.nb > 1 ? 1 : 0);
+    // ordered compaction of this chunk: one list per token for the active_idx
+    // output, and (in shared memory) the chunk's rows active for any token
+    __shared__ int sdown[kMaxChunk];
+    __shared__ int s_ndown;
     const uint32_t m = tid < nrows ? sflag[tid] : 0u;
-    for (int l = 0; l < nlists; ++l) {
-        const int p = l < a.nb ? (int)((m >> l) & 1u) : (int)(m != 0u);
+    for (int l = 0; l < a.nb; ++l) {
+        const int p = (int)((m >> l) & 1u);
         int total;
         const int pos = block_excl_scan(p, scan_tmp, &total);
         if (p) a.lidx[(size_t)l * F + row0 + pos] = row0 + tid;
         if (tid == 0) a.cnt[(size_t)l * a.C + blockIdx.x] = total;
+    }
+    {
+        const int p = m != 0u;
+        int total;
+        const int pos = block_excl_scan(p, scan_tmp, &total);
+        if (p) sdown[pos] = tid;
+        if (tid == 0) s_ndown = total;
+    }
+    __syncthreads();
+
+    // Active neurons of this chunk, in batches that fit the idle ring: their
+    // W_downT rows (and W_up rows unless u_j is known) come from L2 by bulk copy
+    // in one round trip; a warp per row forms u_j and h_j = a_j u_j; then every
+    // thread owns 16-byte column units and accumulates h_j * W_down[:, j] over
+    // the rows in ascending order (deterministic) into this CTA's partial.
+    const int ndown = s_ndown;
+    const int per_row_slots = UP ? 1 : 2;
+    const int cap = (int)((size_t)kGateWarps * D * stage_bytes / row_bytes) / per_row_slots;
+    const char *wd = static_cast<const char *>(a.wdT);
+    const char *wu = static_cast<const char *>(a.wu);
+    const int nwarps = blockDim.x >> 5;
+    for (int b0 = 0, batch = 0;; b0 += cap, ++batch) {
+        const int bn = min(cap, ndown - b0);
+        if (bn > 0) {
+            if (tid == 0) {
+                fence_proxy_async_smem();  // earlier generic reads of the ring precede the copies
+                const uint64_t pol = l2_evict_first_policy();
+                mbar_arrive_expect_tx(dbar, (uint32_t)(bn * per_row_slots) * row_bytes);
+                for (int i = 0; i < bn; ++i) {
+                    const size_t j = (size_t)(row0 + sdown[b0 + i]);
+                    bulk_load(ring + (size_t)i * row_bytes, wd + j * row_bytes, row_bytes, dbar, pol);
+                    if (!UP) bulk_load(ring + (size_t)(cap + i) * row_bytes, wu + j * row_bytes, row_bytes, dbar, pol);
+                }
+            }
+            const bool ok = mbar_wait(dbar, (uint32_t)batch & 1u);
+            if (!__syncthreads_and(ok)) {
+                if (tid == 0) record_error(a.err, SFFN_ERR_TIMEOUT);
+                return;
+            }
+            if (!UP) {
+                for (int i = warp; i < bn; i += nwarps) {
+                    const unsigned char *ur = ring + (size_t)(cap + i) * row_bytes;
+                    float su[NB];
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) su[b] = 0.f;
+                    for (uint32_t u = lane; u < units; u += 32) {
+                        float f[W::E];
+                        W::unpack(*reinterpret_cast<const uint4 *>(ur + u * 16), f);
+#pragma unroll
+                        for (int b = 0; b < NB; ++b) {
+                            float xf[W::E];
+                            W::unpack(xs[(size_t)b * units + u], xf);
+#pragma unroll
+                            for (int e = 0; e < W::E; ++e) su[b] = fmaf(f[e], xf[e], su[b]);
+                        }
+                    }
+                    const int r = sdown[b0 + i];
+#pragma unroll
+                    for (int b = 0; b < NB; ++b) {
+                        const float t = warp_sum(su[b]);
+                        if (lane == b) sh[r][b] *= t;  // h = a_j * u_j
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        for (uint32_t u = tid; u < units; u += blockDim.x) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                if (b >= a.nb) break;
+                float acc[W::E];
+#pragma unroll
+                for (int e = 0; e < W::E; ++e) acc[e] = 0.f;
+                for (int i = 0; i < bn; ++i) {
+                    const float h = sh[sdown[b0 + i]][b];
+                    float f[W::E];
+                    W::unpack(*reinterpret_cast<const uint4 *>(ring + (size_t)i * row_bytes + u * 16), f);
+#pragma unroll
+                    for (int e = 0; e < W::E; ++e) acc[e] = fmaf(h, f[e], acc[e]);
+                }
+                float4 *dst = reinterpret_cast<float4 *>(a.part + ((size_t)blockIdx.x * a.nb + b) * d + u * W::E);
+#pragma unroll
+                for (int q = 0; q < W::E / 4; ++q) {
+                    float4 v = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                    if (batch > 0) {
+                        const float4 o = dst[q];
+                        v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+                    }
+                    dst[q] = v;
+                }
+            }
+        }
+        if (b0 + cap >= ndown) break;
+        __syncthreads();  // the next batch overwrites the ring
     }
 }
 
@@ -226,6 +477,8 @@ constexpr int kSelThreads = 1024;
 struct KeepArgs {
     const float *score;  // [nb, F]
     float *aeff;         // [nb, F] raw act values -> zeroed outside the selection
+    const float *uval;   // [nb, F] u_j when known (gate-and-up score), else null
+    float *lh;           // with uval: h = a * u aligned with the token's list (nb == 1)
     int F, k, nb, C;
     int *cnt, *lidx;
     uint32_t *mask;      // [nb, ceil(F/32)] selection bitmask (nb > 1)
@@ -309,6 +562,7 @@ __global__ void __launch_bounds__(kSelThreads) k_keep_ratio(KeepArgs a) {
         const bool s = kv > T || (kv == T && (unsigned)(eq_base + eq_seen) < take_eq);
         eq_seen += kv == T;
         if (s) {
+            if (a.lh && a.nb == 1) a.lh[pos] = a.aeff[j] * a.uval[j];
             a.lidx[(size_t)b * F + pos++] = j;
             atomicOr(&smask[j >> 5], 1u << (j & 31));
         } else {
@@ -323,7 +577,7 @@ __global__ void __launch_bounds__(kSelThreads) k_keep_ratio(KeepArgs a) {
 
 // union of the per-token keep-ratio selections (nb > 1), ascending
 __global__ void __launch_bounds__(kSelThreads) k_union(const uint32_t *mask, int nb, int F, int C, int *cnt,
-                                                      int *lidx) {
+                                                      int *lidx, const float *aeff, const float *uval, float *lh) {
     __shared__ int tmp[34];
     griddep_wait();
     griddep_launch_dependents();
@@ -344,7 +598,10 @@ __global__ void __launch_bounds__(kSelThreads) k_union(const uint32_t *mask, int
         while (m) {
             const int bit = __ffs(m) - 1;
             m &= m - 1;
-            lidx[(size_t)nb * F + pos++] = w * 32 + bit;
+            const int j = w * 32 + bit;
+            if (lh)  // aeff is already zero where a token did not select j
+                for (int b = 0; b < nb; ++b) lh[(size_t)b * F + pos] = aeff[(size_t)b * F + j] * uval[(size_t)b * F + j];
+            lidx[(size_t)nb * F + pos++] = j;
         }
     }
     for (int c = tid; c < C; c += blockDim.x) cnt[(size_t)nb * C + c] = c == 0 ? tot : 0;
@@ -361,6 +618,8 @@ struct UpDownArgs {
     const int *cnt, *lidx;
     const float *aeff, *uval;  // uval non-null: u_j already known (gate-and-up score)
     float *part;               // [G2, nb, d]
+    int32_t *active_idx;       // nb == 1: the walked list is the token's own list; write it here
+    int32_t *n_active;
 };
 
 constexpr int kMaxC = 2048;     // max gate CTAs (chunks)
@@ -385,10 +644,7 @@ __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
     const int col0 = tid * COLS;
     const bool own = col0 < d;
 
-    for (int i = tid; i < NB * d; i += blockDim.x) {
-        const int b = i / d;
-        xs[i] = b < a.nb ? W::load_x(a.x, (size_t)b * d + (i - b * d)) : 0.f;
-    }
+    stage_x<W>(xs, a.x, a.nb, NB, d);
     griddep_wait();
     griddep_launch_dependents();
 
@@ -417,8 +673,11 @@ __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
             const int mid = (lo + hi + 1) >> 1;
             if (coff[mid] <= p) lo = mid; else hi = mid - 1;
         }
-        srow[q] = lidx[(size_t)lo * a.R + (p - coff[lo])];
+        const int j = lidx[(size_t)lo * a.R + (p - coff[lo])];
+        srow[q] = j;
+        if (a.active_idx) a.active_idx[p] = j;
     }
+    if (a.n_active && blockIdx.x == 0 && tid == 0) a.n_active[0] = n_u;
     __syncthreads();
 
     float acc[NB][COLS];
@@ -523,6 +782,157 @@ __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
 }
 
 // ---------------------------------------------------------------------------
+// sparse down kernel: h_j already known
+// ---------------------------------------------------------------------------
+//
+// Persistent grid.  Each CTA takes an equal share of the walked list's
+// entries (j, h_j[b]), then every thread owns 8 output columns and issues the
+// 16-byte W_downT loads of all its rows at once (one memory round trip for the
+// usual handful of rows per CTA), accumulating h_j * W_down[:, j] in fp32.
+
+struct DownArgs {
+    const void *wdT;
+    int d, F, nb, R, C, list_u;
+    int by_chunk;              // 1: CTA c walks gate chunk c (grid == C); 0: equal shares of the list
+    int max_rows;              // capacity of the row list in shared memory
+    const int *cnt, *lidx;
+    const float *lh;           // [nb, F] aligned with list list_u
+    float *part;               // [G2, nb, d]
+    int32_t *active_idx;       // nb == 1: write the token's list here
+    int32_t *n_active;
+};
+
+constexpr int kDownMaxThreads = 512;
+
+template <class W, int NB>
+__global__ void __launch_bounds__(kDownMaxThreads) k_down(DownArgs a) {
+    constexpr int COLS = 8;
+    constexpr int UPT = COLS / W::E;
+    constexpr int RB = NB <= 2 ? 16 : 8;
+    extern __shared__ int smi[];
+    int *coff = smi;                                   // [C + 1]
+    int *srow = smi + kMaxC + 1;                       // [max_rows]
+    __shared__ int tmp[34];
+    const int tid = threadIdx.x;
+    const int d = a.d, F = a.F;
+    const int col0 = tid * COLS;
+    const bool own = col0 < d;
+    float *shv = reinterpret_cast<float *>(srow + a.max_rows);  // [max_rows][NB]
+
+    griddep_wait();
+    griddep_launch_dependents();
+    const int *cnt = a.cnt + (size_t)a.list_u * a.C;
+    const int *lidx = a.lidx + (size_t)a.list_u * F;
+    int nr;
+    if (a.by_chunk) {
+        // this CTA's rows are exactly gate chunk blockIdx.x: no scan before the loads
+        const int c = blockIdx.x;
+        nr = cnt[c];
+        for (int q = tid; q < nr; q += blockDim.x) {
+            const size_t pos = (size_t)c * a.R + q;
+            srow[q] = lidx[pos];
+            for (int b = 0; b < NB; ++b) shv[q * NB + b] = b < a.nb ? a.lh[(size_t)b * F + pos] : 0.f;
+        }
+        __syncthreads();
+    } else {
+        const int per = (a.C + blockDim.x - 1) / blockDim.x;
+        const int c0 = min(a.C, tid * per), c1 = min(a.C, c0 + per);
+        int s = 0;
+        for (int c = c0; c < c1; ++c) s += cnt[c];
+        int total;
+        int base = block_excl_scan(s, tmp, &total);
+        for (int c = c0; c < c1; ++c) { coff[c] = base; base += cnt[c]; }
+        if (tid == 0) coff[a.C] = total;
+        __syncthreads();
+        const int n_u = coff[a.C];
+        const int p0 = (int)((long long)blockIdx.x * n_u / gridDim.x);
+        const int p1 = (int)((long long)(blockIdx.x + 1) * n_u / gridDim.x);
+        nr = p1 - p0;
+        for (int q = tid; q < nr; q += blockDim.x) {
+            const int p = p0 + q;
+            int lo = 0, hi = a.C - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (coff[mid] <= p) lo = mid; else hi = mid - 1;
+            }
+            const size_t pos = (size_t)lo * a.R + (p - coff[lo]);
+            const int j = lidx[pos];
+            srow[q] = j;
+            for (int b = 0; b < NB; ++b) shv[q * NB + b] = b < a.nb ? a.lh[(size_t)b * F + pos] : 0.f;
+            if (a.active_idx) a.active_idx[p] = j;
+        }
+        if (a.n_active && blockIdx.x == 0 && tid == 0) a.n_active[0] = n_u;
+        __syncthreads();
+    }
+
+    float acc[NB][COLS];
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int e = 0; e < COLS; ++e) acc[b][e] = 0.f;
+    const size_t row_bytes = (size_t)d * 16 / W::E;
+    // all threads run the same control flow (the scan below has barriers);
+    // threads beyond the last column only skip their loads and stores
+    for (int g0 = 0; g0 < nr; g0 += RB) {
+        uint4 dn[RB][UPT];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            if (own && g0 + r < nr) {
+                const char *pd = static_cast<const char *>(a.wdT) + (size_t)srow[g0 + r] * row_bytes +
+                                 (size_t)col0 * 16 / W::E;
+#pragma unroll
+                for (int q = 0; q < UPT; ++q) dn[r][q] = ldg_stream(pd + q * 16);
+            } else {
+#pragma unroll
+                for (int q = 0; q < UPT; ++q) dn[r][q] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        if (a.by_chunk && g0 == 0) {
+            // while the first loads are in flight: this chunk's position in the
+            // token's ascending list = exclusive prefix of the earlier chunks' counts
+            int sacc = 0;
+            for (int c = tid; c < (int)blockIdx.x; c += blockDim.x) sacc += cnt[c];
+            int total;
+            block_excl_scan(sacc, tmp, &total);
+            if (a.active_idx)
+                for (int q = tid; q < nr; q += blockDim.x) a.active_idx[total + q] = srow[q];
+            if (a.n_active && blockIdx.x == gridDim.x - 1 && tid == 0) a.n_active[0] = total + nr;
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+            if (g0 + r < nr) {
+                float fd[COLS];
+#pragma unroll
+                for (int q = 0; q < UPT; ++q) W::unpack(dn[r][q], fd + q * W::E);
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const float h = shv[(g0 + r) * NB + b];
+#pragma unroll
+                    for (int e = 0; e < COLS; ++e) acc[b][e] = fmaf(h, fd[e], acc[b][e]);
+                }
+            }
+        }
+    }
+    if (a.by_chunk && nr == 0) {  // no rows: still publish this chunk's list position
+        int sacc = 0;
+        for (int c = tid; c < (int)blockIdx.x; c += blockDim.x) sacc += cnt[c];
+        int total;
+        block_excl_scan(sacc, tmp, &total);
+        if (a.n_active && blockIdx.x == gridDim.x - 1 && tid == 0) a.n_active[0] = total;
+    }
+    if (own) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            if (b < a.nb) {
+                float4 *dst = reinterpret_cast<float4 *>(a.part + ((size_t)blockIdx.x * a.nb + b) * d + col0);
+                dst[0] = make_float4(acc[b][0], acc[b][1], acc[b][2], acc[b][3]);
+                dst[1] = make_float4(acc[b][4], acc[b][5], acc[b][6], acc[b][7]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // reduction of the partials + per-token active lists
 // ---------------------------------------------------------------------------
 
@@ -531,50 +941,45 @@ struct ReduceArgs {
     int G2, nb, d;
     void *out;
     int out_f32;
-    int n_red;                 // CTAs doing the column reduction; the next nb write lists
+    int n_red;                 // CTAs doing the column reduction; the next ones write per-token lists
     int C, R, F;
     const int *cnt, *lidx;
     int32_t *active_idx, *n_active;
 };
 
 __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
-    __shared__ float4 red[8][32];
+    __shared__ float red[8][32];
     __shared__ int tmp[34];
     __shared__ int coff[kMaxC + 1];
     griddep_wait();
-    // last kernel of the call: no early trigger, so the next call sees all writes
+    // The next call's first kernel may start now: before its own dependency
+    // wait it only streams weights, which no kernel of this library writes.
+    griddep_launch_dependents();
     const int tid = threadIdx.x;
     if ((int)blockIdx.x < a.n_red) {
+        // 32 consecutive outputs per CTA; 8 groups each sum every 8th partial
+        // (fixed assignment and order: deterministic)
         const int lane = tid & 31, grp = tid >> 5;
         const size_t total = (size_t)a.nb * a.d;
-        const size_t c4 = (size_t)blockIdx.x * 128 + lane * 4;
-        float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c4 < total) {
-            for (int c = grp; c < a.G2; c += 8) {
-                const float4 v = *reinterpret_cast<const float4 *>(a.part + (size_t)c * total + c4);
-                s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
-            }
+        const size_t c = (size_t)blockIdx.x * 32 + lane;
+        float s = 0.f;
+        if (c < total) {
+#pragma unroll 8
+            for (int p = grp; p < a.G2; p += 8) s += a.part[(size_t)p * total + c];
         }
         red[grp][lane] = s;
         __syncthreads();
-        if (grp == 0 && c4 < total) {
-            float4 t = red[0][lane];
-            for (int g = 1; g < 8; ++g) {
-                const float4 v = red[g][lane];
-                t.x += v.x; t.y += v.y; t.z += v.z; t.w += v.w;
-            }
-            if (a.out_f32) {
-                *reinterpret_cast<float4 *>(static_cast<float *>(a.out) + c4) = t;
-            } else {
-                uint2 o;
-                o.x = (uint32_t)f32_to_bf16_bits(t.x) | ((uint32_t)f32_to_bf16_bits(t.y) << 16);
-                o.y = (uint32_t)f32_to_bf16_bits(t.z) | ((uint32_t)f32_to_bf16_bits(t.w) << 16);
-                *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(a.out) + c4) = o;
-            }
+        if (grp == 0 && c < total) {
+            float t = red[0][lane];
+#pragma unroll
+            for (int g = 1; g < 8; ++g) t += red[g][lane];
+            if (a.out_f32) static_cast<float *>(a.out)[c] = t;
+            else static_cast<uint16_t *>(a.out)[c] = f32_to_bf16_bits(t);
         }
         return;
     }
-    // per-token list: scan the chunk counts, then copy the chunks in order
+    // per-token list (nb > 1): scan the chunk counts, then every thread maps
+    // output positions to (chunk, offset) by binary search -- no serial chain
     const int b = blockIdx.x - a.n_red;
     const int *cnt = a.cnt + (size_t)b * a.C;
     const int per = (a.C + blockDim.x - 1) / blockDim.x;
@@ -585,11 +990,15 @@ __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
     int base = block_excl_scan(s, tmp, &total);
     for (int c = c0; c < c1; ++c) { coff[c] = base; base += cnt[c]; }
     __syncthreads();
-    const int *lidx = a.lidx + (size_t)b * a.F;
-    int32_t *dst = a.active_idx + (size_t)b * a.F;
-    for (int c = 0; c < a.C; ++c) {
-        const int n = (c + 1 < a.C ? coff[c + 1] : total) - coff[c];
-        for (int i = tid; i < n; i += blockDim.x) dst[coff[c] + i] = lidx[(size_t)c * a.R + i];
+    const int *__restrict__ lidx = a.lidx + (size_t)b * a.F;
+    int32_t *__restrict__ dst = a.active_idx + (size_t)b * a.F;
+    for (int p = tid; p < total; p += blockDim.x) {
+        int lo = 0, hi = a.C - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (coff[mid] <= p) lo = mid; else hi = mid - 1;
+        }
+        dst[p] = lidx[(size_t)lo * a.R + (p - coff[lo])];
     }
     if (tid == 0) a.n_active[b] = total;
 }
@@ -604,7 +1013,7 @@ DecodePlan make_decode_plan(int B, int d, int F) {
     p.d = d;
     p.F = F;
     const int sms = device_sm_count();
-    int C = 2 * sms;
+    int C = sms;                         // one gate CTA per SM
     if (C > F) C = F;
     int R = (F + C - 1) / C;
     if (R > kMaxChunk) R = kMaxChunk;
@@ -617,13 +1026,41 @@ DecodePlan make_decode_plan(int B, int d, int F) {
     p.off_err = o; o = align_up(o + sizeof(int32_t));
     p.off_cnt = o; o = align_up(o + sizeof(int) * (size_t)p.nlists * p.C);
     p.off_lidx = o; o = align_up(o + sizeof(int) * (size_t)p.nlists * F);
+    p.off_lh = o; o = align_up(o + sizeof(float) * (size_t)B * F);
     p.off_aeff = o; o = align_up(o + sizeof(float) * (size_t)B * F);
     p.off_uval = o; o = align_up(o + sizeof(float) * (size_t)B * F);
     p.off_score = o; o = align_up(o + sizeof(float) * (size_t)B * F);
     p.off_mask = o; o = align_up(o + sizeof(uint32_t) * (size_t)B * ((F + 31) / 32));
-    p.off_part = o; o = align_up(o + sizeof(float) * (size_t)p.G2 * B * d);
+    p.off_part = o; o = align_up(o + sizeof(float) * (size_t)(p.G2 > p.C ? p.G2 : p.C) * B * d);
     p.total = o;
     return p;
+}
+
+// Dynamic shared memory of the gate kernel with D rows in flight per warp.
+static size_t gate_smem(int NB, uint32_t row_bytes, uint32_t stage_bytes, int D) {
+    return (size_t)kGateWarps * D * stage_bytes + (size_t)NB * row_bytes +
+           sizeof(uint64_t) * ((size_t)kGateWarps * D + 1);
+}
+
+template <class W, int NB, bool UP>
+static cudaError_t launch_gate(const GateArgs &ga_in, const DecodePlan &p, cudaStream_t s) {
+    GateArgs ga = ga_in;
+    const uint32_t row_bytes = (uint32_t)(p.d / W::E) * 16u;
+    const uint32_t stage_bytes = (UP ? 2u : 1u) * row_bytes;
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, (const void *)k_gate<W, NB, UP>);
+    if (e != cudaSuccess) return e;
+    const long avail = (long)device_smem_optin() - (long)fa.sharedSizeBytes - 1024 - (long)NB * row_bytes - 16;
+    long D = avail / ((long)kGateWarps * (stage_bytes + sizeof(uint64_t)));
+    if (D > 4) D = 4;
+    const int rows_per_warp = (p.R + kGateWarps - 1) / kGateWarps;
+    if (D > rows_per_warp) D = rows_per_warp;
+    if (D < 1) return cudaErrorInvalidConfiguration;
+    ga.stages = (int)D;
+    const size_t smem = gate_smem(NB, row_bytes, stage_bytes, ga.stages);
+    e = set_max_smem((const void *)k_gate<W, NB, UP>, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_k(k_gate<W, NB, UP>, dim3(p.C), dim3(kGateThreads), smem, s, ga);
 }
 
 template <class W, int NB>
@@ -633,8 +1070,10 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     const bool scores_only = c.scores_only != nullptr;
     const bool keep = c.mode == SFFN_MODE_KEEP_RATIO;
     const bool up = c.score == SFFN_SCORE_GATE_UP && (c.mode != SFFN_MODE_EXACT || scores_only);
+    int32_t *err = reinterpret_cast<int32_t *>(ws + p.off_err);
     int *cnt = reinterpret_cast<int *>(ws + p.off_cnt);
     int *lidx = reinterpret_cast<int *>(ws + p.off_lidx);
+    float *lh = reinterpret_cast<float *>(ws + p.off_lh);
     float *aeff = reinterpret_cast<float *>(ws + p.off_aeff);
     float *uval = reinterpret_cast<float *>(ws + p.off_uval);
     float *score = reinterpret_cast<float *>(ws + p.off_score);
@@ -657,26 +1096,32 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     ga.score_kind = c.score;
     ga.tau = c.param;
     ga.decide = (!scores_only && !keep) ? 1 : 0;
-    ga.aeff = scores_only ? nullptr : aeff;
-    ga.uval = up && !scores_only ? uval : nullptr;
+    ga.list_u = p.list_u;
+    ga.aeff = (keep && !scores_only) ? aeff : nullptr;
+    ga.uval = (keep && up && !scores_only) ? uval : nullptr;
     ga.score = scores_only ? c.scores_only : (keep ? score : nullptr);
     ga.cnt = cnt;
     ga.lidx = lidx;
-    const size_t smem_gate = sizeof(float) * NB * p.d;
-    cudaError_t e;
-    if (up) {
-        e = set_max_smem((const void *)k_gate<W, NB, true>, (int)smem_gate);
-        if (e == cudaSuccess) e = launch_k(k_gate<W, NB, true>, dim3(p.C), dim3(kGateThreads), smem_gate, s, ga);
-    } else {
-        e = set_max_smem((const void *)k_gate<W, NB, false>, (int)smem_gate);
-        if (e == cudaSuccess) e = launch_k(k_gate<W, NB, false>, dim3(p.C), dim3(kGateThreads), smem_gate, s, ga);
-    }
+    ga.lh = lh;
+    ga.err = err;
+    ga.wdT = w->w_downT;
+    ga.part = part;
+    cudaError_t e = up ? launch_gate<W, NB, true>(ga, p, s) : launch_gate<W, NB, false>(ga, p, s);
     if (e != cudaSuccess || scores_only) return e;
 
+    int nparts = p.G2;
+    bool list_ctas = p.nb > 1;
+    if (!keep) {  // exact / threshold: the gate kernel already wrote per-chunk partials
+        nparts = p.C;
+        list_ctas = true;
+    }
+    bool have_h = up;  // keep-ratio: h_j known before the down pass
     if (keep) {
         KeepArgs ka = {};
         ka.score = score;
         ka.aeff = aeff;
+        ka.uval = up ? uval : nullptr;
+        ka.lh = up ? lh : nullptr;
         ka.F = p.F;
         double kk = floor((double)p.F * (double)c.param);
         int k = kk < 1.0 ? 1 : (int)kk;
@@ -690,46 +1135,68 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
         e = launch_k(k_keep_ratio, dim3(p.nb), dim3(kSelThreads), 0, s, ka);
         if (e != cudaSuccess) return e;
         if (p.nb > 1) {
-            e = launch_k(k_union, dim3(1), dim3(kSelThreads), 0, s, (const uint32_t *)mask, p.nb, p.F, p.C, cnt, lidx);
+            e = launch_k(k_union, dim3(1), dim3(kSelThreads), 0, s, (const uint32_t *)mask, p.nb, p.F, p.C, cnt, lidx,
+                         (const float *)aeff, (const float *)uval, up ? lh : (float *)nullptr);
             if (e != cudaSuccess) return e;
         }
     }
 
-    UpDownArgs ua = {};
-    ua.wu = w->w_up;
-    ua.wdT = w->w_downT;
-    ua.x = c.x;
-    ua.d = p.d;
-    ua.F = p.F;
-    ua.nb = p.nb;
-    ua.R = p.R;
-    ua.C = p.C;
-    ua.list_u = p.list_u;
-    ua.cnt = cnt;
-    ua.lidx = lidx;
-    ua.aeff = aeff;
-    ua.uval = up ? uval : nullptr;
-    ua.part = part;
     const int threads = ((p.d / 8) + 31) / 32 * 32;
     const int max_rows = (p.F + p.G2 - 1) / p.G2 + 1;
-    const size_t smem_ud = sizeof(float) * NB * p.d + sizeof(int) * (kMaxC + 1 + max_rows);
-    if (up) {
-        e = set_max_smem((const void *)k_updown<W, NB, true>, (int)smem_ud);
-        if (e == cudaSuccess) e = launch_k(k_updown<W, NB, true>, dim3(p.G2), dim3(threads), smem_ud, s, ua);
+    if (!keep) {
+        // nothing between the gate kernel and the reduction
+    } else if (have_h) {
+        DownArgs da = {};
+        da.wdT = w->w_downT;
+        da.d = p.d;
+        da.F = p.F;
+        da.nb = p.nb;
+        da.R = p.R;
+        da.C = p.C;
+        da.list_u = p.list_u;
+        da.cnt = cnt;
+        da.lidx = lidx;
+        da.lh = lh;
+        da.part = part;
+        da.active_idx = p.nb == 1 ? c.active_idx : nullptr;
+        da.n_active = p.nb == 1 ? c.n_active : nullptr;
+        da.by_chunk = 0;  // keep-ratio lists are one block, not per gate chunk
+        da.max_rows = max_rows;
+        const size_t smem = sizeof(int) * (kMaxC + 1 + da.max_rows) + sizeof(float) * (size_t)da.max_rows * NB;
+        e = set_max_smem((const void *)k_down<W, NB>, (int)smem);
+        if (e == cudaSuccess) e = launch_k(k_down<W, NB>, dim3(nparts), dim3(threads), smem, s, da);
     } else {
-        e = set_max_smem((const void *)k_updown<W, NB, false>, (int)smem_ud);
-        if (e == cudaSuccess) e = launch_k(k_updown<W, NB, false>, dim3(p.G2), dim3(threads), smem_ud, s, ua);
+        UpDownArgs ua = {};
+        ua.wu = w->w_up;
+        ua.wdT = w->w_downT;
+        ua.x = c.x;
+        ua.d = p.d;
+        ua.F = p.F;
+        ua.nb = p.nb;
+        ua.R = p.R;
+        ua.C = p.C;
+        ua.list_u = p.list_u;
+        ua.cnt = cnt;
+        ua.lidx = lidx;
+        ua.aeff = aeff;
+        ua.uval = nullptr;
+        ua.part = part;
+        ua.active_idx = p.nb == 1 ? c.active_idx : nullptr;
+        ua.n_active = p.nb == 1 ? c.n_active : nullptr;
+        const size_t smem = sizeof(float) * NB * p.d + sizeof(int) * (kMaxC + 1 + max_rows);
+        e = set_max_smem((const void *)k_updown<W, NB, false>, (int)smem);
+        if (e == cudaSuccess) e = launch_k(k_updown<W, NB, false>, dim3(p.G2), dim3(threads), smem, s, ua);
     }
     if (e != cudaSuccess) return e;
 
     ReduceArgs ra = {};
     ra.part = part;
-    ra.G2 = p.G2;
+    ra.G2 = nparts;
     ra.nb = p.nb;
     ra.d = p.d;
     ra.out = c.out;
     ra.out_f32 = w->wdtype == SFFN_F32;
-    ra.n_red = (int)(((size_t)p.nb * p.d + 127) / 128);
+    ra.n_red = (int)(((size_t)p.nb * p.d + 31) / 32);
     ra.C = p.C;
     ra.R = p.R;
     ra.F = p.F;
@@ -738,7 +1205,7 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     ra.active_idx = c.active_idx;
     ra.n_active = c.n_active;
     // keep-ratio lists live in chunk 0 of each token (chunk stride irrelevant there)
-    return launch_k(k_reduce, dim3(ra.n_red + p.nb), dim3(256), 0, s, ra);
+    return launch_k(k_reduce, dim3(ra.n_red + (list_ctas ? p.nb : 0)), dim3(256), 0, s, ra);
 }
 
 template <class W>

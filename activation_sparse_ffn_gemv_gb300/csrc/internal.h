@@ -7,7 +7,7 @@
 
 #include <utility>
 
-#include "../../include/sffn.h"
+#include "sffn.h"
 
 namespace sffn {
 
@@ -16,6 +16,8 @@ inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a
 
 // SM count of the current device (cached per device).
 int device_sm_count();
+// Opt-in shared memory per block of the current device (cached per device).
+int device_smem_optin();
 // Opt a kernel into more than 48 KB of dynamic shared memory (once per device).
 cudaError_t set_max_smem(const void *kernel, int bytes);
 
@@ -50,7 +52,7 @@ struct DecodePlan {
     int nlists;   // nb per-token lists (+1 union list when nb > 1)
     int list_u;   // index of the list the up/down kernel walks
     // workspace offsets (bytes)
-    size_t off_err, off_cnt, off_lidx, off_aeff, off_uval, off_score, off_mask, off_part, total;
+    size_t off_err, off_cnt, off_lidx, off_lh, off_aeff, off_uval, off_score, off_mask, off_part, total;
 };
 
 DecodePlan make_decode_plan(int B, int d, int F);
