@@ -411,26 +411,41 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
                 return;
             }
             if (!UP) {
+                constexpr int UPL = W::E == 8 ? 16 : 32;  // units per lane (d_model <= 4096)
                 for (int i = warp; i < bn; i += nwarps) {
                     const unsigned char *ur = ring + (size_t)(cap + i) * row_bytes;
-                    float su[NB];
+                    float su[NB][4];
 #pragma unroll
-                    for (int b = 0; b < NB; ++b) su[b] = 0.f;
-                    for (uint32_t u = lane; u < units; u += 32) {
-                        float f[W::E];
-                        W::unpack(*reinterpret_cast<const uint4 *>(ur + u * 16), f);
+                    for (int b = 0; b < NB; ++b)
 #pragma unroll
-                        for (int b = 0; b < NB; ++b) {
-                            float xf[W::E];
-                            W::unpack(xs[(size_t)b * units + u], xf);
+                        for (int c = 0; c < 4; ++c) su[b][c] = 0.f;
 #pragma unroll
-                            for (int e = 0; e < W::E; ++e) su[b] = fmaf(f[e], xf[e], su[b]);
+                    for (int i0 = 0; i0 < UPL; i0 += 4) {
+                        uint4 v[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t u = (i0 + c) * 32 + lane;
+                            v[c] = u < units ? *reinterpret_cast<const uint4 *>(ur + u * 16) : make_uint4(0, 0, 0, 0);
                         }
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint32_t u = (i0 + c) * 32 + lane;
+                            float f[W::E];
+                            W::unpack(v[c], f);
+#pragma unroll
+                            for (int b = 0; b < NB; ++b) {
+                                float xf[W::E];
+                                W::unpack(u < units ? xs[(size_t)b * units + u] : make_uint4(0, 0, 0, 0), xf);
+#pragma unroll
+                                for (int e = 0; e < W::E; ++e) su[b][c] = fmaf(f[e], xf[e], su[b][c]);
+                            }
+                        }
+                        if ((i0 + 4) * 32 >= (int)units) break;
                     }
                     const int r = sdown[b0 + i];
 #pragma unroll
                     for (int b = 0; b < NB; ++b) {
-                        const float t = warp_sum(su[b]);
+                        const float t = warp_sum((su[b][0] + su[b][1]) + (su[b][2] + su[b][3]));
                         if (lane == b) sh[r][b] *= t;  // h = a_j * u_j
                     }
                 }
@@ -623,6 +638,7 @@ struct UpDownArgs {
 };
 
 constexpr int kMaxC = 2048;     // max gate CTAs (chunks)
+constexpr int kListChunks = 8;  // chunks per list-writing CTA of the reduction
 
 constexpr int kUpDownMaxThreads = 512;   // d_model <= 4096 at 8 columns per thread
 
@@ -950,7 +966,6 @@ struct ReduceArgs {
 __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
     __shared__ float red[8][32];
     __shared__ int tmp[34];
-    __shared__ int coff[kMaxC + 1];
     griddep_wait();
     // The next call's first kernel may start now: before its own dependency
     // wait it only streams weights, which no kernel of this library writes.
@@ -978,29 +993,42 @@ __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
         }
         return;
     }
-    // per-token list (nb > 1): scan the chunk counts, then every thread maps
-    // output positions to (chunk, offset) by binary search -- no serial chain
-    const int b = blockIdx.x - a.n_red;
+    // Per-token ascending lists: each list CTA owns kListChunks consecutive
+    // chunks of one token; its offset is the sum of the earlier chunks' counts
+    // (a warp-parallel sum), then a warp per chunk copies the chunk's entries.
+    const int li = blockIdx.x - a.n_red;
+    const int groups = (a.C + kListChunks - 1) / kListChunks;
+    const int b = li / groups, grp = li - b * groups;
+    const int c0 = grp * kListChunks, c1 = min(a.C, c0 + kListChunks);
     const int *cnt = a.cnt + (size_t)b * a.C;
-    const int per = (a.C + blockDim.x - 1) / blockDim.x;
-    const int c0 = min(a.C, tid * per), c1 = min(a.C, c0 + per);
     int s = 0;
-    for (int c = c0; c < c1; ++c) s += cnt[c];
-    int total;
-    int base = block_excl_scan(s, tmp, &total);
-    for (int c = c0; c < c1; ++c) { coff[c] = base; base += cnt[c]; }
-    __syncthreads();
-    const int *__restrict__ lidx = a.lidx + (size_t)b * a.F;
-    int32_t *__restrict__ dst = a.active_idx + (size_t)b * a.F;
-    for (int p = tid; p < total; p += blockDim.x) {
-        int lo = 0, hi = a.C - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (coff[mid] <= p) lo = mid; else hi = mid - 1;
+    for (int c = tid; c < c0; c += blockDim.x) s += cnt[c];
+    int base;
+    block_excl_scan(s, tmp, &base);   // base = total over the CTA = offset of chunk c0
+    const int lane = tid & 31, wp = tid >> 5;
+    __shared__ int ccnt[kListChunks], coffs[kListChunks];
+    if (tid == 0) {
+        int o = base;
+        for (int c = c0; c < c1; ++c) {
+            ccnt[c - c0] = cnt[c];
+            coffs[c - c0] = o;
+            o += cnt[c];
         }
-        dst[p] = lidx[(size_t)lo * a.R + (p - coff[lo])];
+        if (c1 == a.C) a.n_active[b] = o;
     }
-    if (tid == 0) a.n_active[b] = total;
+    __syncthreads();
+    const int *lidx = a.lidx + (size_t)b * a.F;
+    int32_t *dst = a.active_idx + (size_t)b * a.F;
+    for (int c = c0 + wp; c < c1; c += blockDim.x >> 5) {
+        const int n = ccnt[c - c0], o = coffs[c - c0];
+        if (n <= 128)
+            for (int i = lane; i < n; i += 32) dst[o + i] = lidx[(size_t)c * a.R + i];
+    }
+    for (int c = c0; c < c1; ++c) {  // long lists (keep-ratio: the whole list sits in chunk 0)
+        const int n = ccnt[c - c0], o = coffs[c - c0];
+        if (n > 128)
+            for (int i = tid; i < n; i += blockDim.x) dst[o + i] = lidx[(size_t)c * a.R + i];
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1205,7 +1233,8 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     ra.active_idx = c.active_idx;
     ra.n_active = c.n_active;
     // keep-ratio lists live in chunk 0 of each token (chunk stride irrelevant there)
-    return launch_k(k_reduce, dim3(ra.n_red + (list_ctas ? p.nb : 0)), dim3(256), 0, s, ra);
+    const int list_grid = list_ctas ? p.nb * ((p.C + kListChunks - 1) / kListChunks) : 0;
+    return launch_k(k_reduce, dim3(ra.n_red + list_grid), dim3(256), 0, s, ra);
 }
 
 template <class W>
