@@ -4,22 +4,6 @@
 
 namespace sffn {
 
-SelectPlan make_select_plan(int L, int d) {
-    SelectPlan p = {};
-    p.L = L;
-    p.d = d;
-    size_t o = 0;
-    p.off_err = o; o = align_up(o + sizeof(int32_t));
-    p.off_norms = o; o = align_up(o + sizeof(float) * (size_t)L);
-    p.total = o;
-    return p;
-}
-
-sffn_status run_token_select(const void *, int, int, float, int, int, int32_t *, int32_t *, void *,
-                             const SelectPlan &, cudaStream_t) {
-    return SFFN_ERR_UNSUPPORTED;
-}
-
 PrefillPlan make_prefill_plan(int L, int d, int F) {
     PrefillPlan p = {};
     p.L = L;

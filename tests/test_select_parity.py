@@ -1,0 +1,111 @@
+"""GPU parity of sffn_token_select against the fp64 oracle: the selected set is
+bit-exact except for tokens whose importance lies within 1e-6 (relative) of a
+cut of the selection (the crossing value of the mass prefix or of the
+min_keep extension)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from activation_sparse_ffn_gemv_gb300 import workloads as W
+from tests.oracle_io import mat_from_act
+from tests.parity import TIE_REL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sffn():
+    from activation_sparse_ffn_gemv_gb300 import sffn as S
+    S.lib()
+    return S
+
+
+def _oracle_cuts(s, sel, pre, L, recent_n):
+    """Importance values at which the oracle's selection was cut."""
+    cuts = []
+    if len(pre) and len(pre) < L:
+        cuts.append(s[pre].min())
+    tail = set(range(max(0, L - recent_n), L))
+    ext = [t for t in sel.tolist() if t not in set(pre.tolist()) and t not in tail]
+    if ext:
+        cuts.append(s[ext].min())
+    return cuts
+
+
+def check_select(sffn, ya_cpu: torch.Tensor, m: float, recent_n: int, min_keep: int):
+    L = ya_cpu.shape[0]
+    sel_g, n_g = sffn.token_select(ya_cpu.cuda(), m, recent_n, min_keep)
+    torch.cuda.synchronize()
+    n = int(n_g.item())
+    g = sel_g[:n].cpu().numpy()
+    assert n >= 1 or L == 0
+    assert np.all(np.diff(g) > 0) and (n == 0 or (g[0] >= 0 and g[-1] < L))
+    s = O.token_norms(mat_from_act(ya_cpu))
+    sel, pre = O.mass_select(s, m, recent_n, min_keep)
+    # guards hold on the GPU result itself
+    assert set(range(max(0, L - recent_n), L)) <= set(g.tolist())
+    assert n >= min(min_keep, L)
+    diff = np.setxor1d(g, sel)
+    if diff.size:
+        cuts = _oracle_cuts(s, sel, pre, L, recent_n)
+        ok = np.zeros(diff.size, bool)
+        for c in cuts:
+            ok |= np.abs(s[diff] - c) <= TIE_REL * np.maximum(c, s[diff])
+        assert ok.all(), (f"{(~ok).sum()} tokens differ outside the tie band: {diff[~ok][:8]} "
+                          f"s={s[diff[~ok][:8]]} cuts={cuts}")
+    return g, sel, s
+
+
+@pytest.mark.parametrize("m", [0.2, 0.5, 0.7, 1.0])
+def test_config_prefill_selection_full(sffn, m):
+    c = W.CONFIGS[5]
+    _, ya = W.make_prefill_inputs(c["L"], c["d_model"], seed=0)
+    g, sel, s = check_select(sffn, ya, m, c["recent_n"], c["min_keep"])
+    if m == 1.0:
+        assert g.size == c["L"]
+
+
+@pytest.mark.parametrize("L", [1, 2, 7, 100, 1023, 1024, 1025, 4099])
+@pytest.mark.parametrize("m", [0.0, 1e-9, 0.3, 0.9])
+def test_lengths_and_thresholds(sffn, L, m):
+    _, ya = W.make_prefill_inputs(L, 64, seed=L)
+    check_select(sffn, ya, m, recent_n=5, min_keep=1)
+
+
+def test_all_zero_is_dense(sffn):
+    ya = torch.zeros(300, 64, dtype=torch.bfloat16)
+    g, _, _ = check_select(sffn, ya, 0.4, recent_n=4, min_keep=1)
+    assert g.tolist() == list(range(300))
+
+
+def test_single_nonzero_token(sffn):
+    ya = torch.zeros(500, 64, dtype=torch.bfloat16)
+    ya[123, 5] = 3.0
+    g, _, _ = check_select(sffn, ya, 0.5, recent_n=0, min_keep=1)
+    assert g.tolist() == [123]
+
+
+def test_ties_take_lower_indices(sffn):
+    # identical rows: identical importances; the prefix takes the lowest indices
+    row = torch.randn(1, 64).to(torch.bfloat16)
+    ya = row.repeat(40, 1)
+    g, sel, _ = check_select(sffn, ya, 0.25, recent_n=0, min_keep=1)
+    assert g.tolist() == sel.tolist() == list(range(10))
+
+
+def test_recent_tail_longer_than_sequence(sffn):
+    _, ya = W.make_prefill_inputs(50, 64, seed=3)
+    g, _, _ = check_select(sffn, ya, 0.2, recent_n=128, min_keep=1)
+    assert g.tolist() == list(range(50))
+
+
+@pytest.mark.parametrize("min_keep", [1, 17, 500])
+def test_min_keep_extension(sffn, min_keep):
+    _, ya = W.make_prefill_inputs(1000, 64, seed=9)
+    g, _, _ = check_select(sffn, ya, 0.0, recent_n=0, min_keep=min_keep)
+    assert g.size == min_keep
+    g2, _, _ = check_select(sffn, ya, 0.05, recent_n=3, min_keep=min_keep)
+    assert g2.size >= min_keep
