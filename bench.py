@@ -8,8 +8,11 @@ weights, far larger than L2, so no L2 flush is needed).  A step is one CUDA
 graph of 1024 sffn_decode calls (gate -> sparse up/down -> reduce each).
 
 Prints one JSON line (rank 0).  `value` is decode microseconds per token over
-all ranks' tokens (lower is better).  `--impl reference` times the fp64 CPU
-oracle on a bounded sample of the same workload instead.
+all ranks' tokens (lower is better).  The `prefill` object adds the second half
+of the metric: token-selective prefill (L 16384, d_model 5120, d_ff 25600,
+SwiGLU bf16) tokens/s for mass_thresh 0.2 / 0.5 / 0.7 / 1.0 and the tensor
+roofline of its FFN GEMMs.  `--impl reference` times the fp64 CPU oracle on a
+bounded sample of the decode workload instead.
 """
 from __future__ import annotations
 
@@ -237,7 +240,7 @@ def run_ours(args):
     value = ms_max * 1e3 / total_tokens
     hbm, bf16_peak, bf16_sus, peak_src = peaks()
     achieved = bytes_tok / (us_tok * 1e-6) / 1e9
-    kernels_per_call = 3
+    kernels_per_call = 2  # fused gate/down kernel + reduction
     res = None
     if rank == 0:
         res = {
@@ -252,10 +255,10 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "active_fraction": round(a, 5),
             "gbps": round(achieved, 1),
-            "roofline": {"bound": "hbm", "kernel": "sffn_decode call (gate + sparse up/down + reduce)",
+            "roofline": {"bound": "hbm", "kernel": "sffn_decode call (gate+sparse up/down kernel, reduction)",
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peak_src,
-                         "bytes_per_launch": round(bytes_tok), "traffic": None},
+                         "bytes_per_launch": round(bytes_tok), "traffic": traffic_for("decode_exact_llama")},
             "e2e": {"value": round(ms_e2e * 1e3 / total_tokens, 4), "unit": "us/token",
                     "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
                     "d2h_bytes_per_step": int(outh.numel() * outh.element_size() + nh.numel() * 4)},
@@ -265,10 +268,125 @@ def run_ours(args):
     # CPU baseline: the oracle on a bounded sample of the same workload
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(layers[0], x[: args.cpu_tokens].cpu())
+    del graph, graph_e2e, layers, ws_list, idx, work
+    torch.cuda.empty_cache()
+    if not args.no_prefill:
+        pf = bench_prefill(args, dev, rank, world, dist)
+        if rank == 0:
+            res["prefill"] = pf
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     return res
+
+
+def traffic_for(key):
+    """DRAM bytes per launch from a committed ncu capture, or None if the kernel
+    sources changed since it was taken (profiles/traffic.json holds the hash)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(key)
+        if not e:
+            return None
+        h = hashlib.sha256()
+        for f in e["sources"]:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        return e["bytes"] if h.hexdigest() == e["sha256"] else None
+    except Exception:
+        return None
+
+
+def bench_prefill(args, dev, rank, world, dist):
+    """Token-selective prefill (L 16384, d_model 5120, d_ff 25600, SwiGLU bf16):
+    token selection + the selected-token FFN, at each mass threshold."""
+    import torch
+
+    from activation_sparse_ffn_gemv_gb300 import sffn
+    from activation_sparse_ffn_gemv_gb300 import workloads as W
+    c = W.CONFIGS[5]
+    L, d, F = c["L"], c["d_model"], c["d_ff"]
+    layer = W.make_ffn_layer(5, seed=7 + rank, device=dev)
+    X, Ya = W.make_prefill_inputs(L, d, seed=rank, device=dev)
+    w = sffn.Weights(layer)
+    ws_sel = sffn.alloc_workspace(sffn.WS_SELECT, L, None, dev)
+    ws_pf = sffn.alloc_workspace(sffn.WS_PREFILL, L, w, dev)
+    sel = torch.empty(L, dtype=torch.int32, device=dev)
+    n = torch.empty(1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(X)
+    stream = torch.cuda.Stream(device=dev)
+    _, bf16_peak, _, peak_src = peaks()
+    rows = {}
+    for m in c["mass"]:
+        def sel_call():
+            sffn.token_select(Ya, m, c["recent_n"], c["min_keep"], sel_idx=sel, n_sel=n, workspace=ws_sel,
+                              stream=stream)
+
+        def ffn_call():
+            sffn.prefill(X, Ya, w, sel, n, out=out, workspace=ws_pf, stream=stream)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                sel_call()
+                ffn_call()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * args.prefill_steps + 1)]
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(args.prefill_steps):
+                sel_call()
+                ev[2 * i + 1].record(stream)
+                ffn_call()
+                ev[2 * i + 2].record(stream)
+        ev[-1].synchronize()
+        t_sel = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.prefill_steps)) / args.prefill_steps
+        t_ffn = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.prefill_steps)) / args.prefill_steps
+        t_tot = ev[0].elapsed_time(ev[-1]) / args.prefill_steps
+        if dist is not None:
+            t = torch.tensor([t_tot, t_ffn, t_sel], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            t_tot, t_ffn, t_sel = (float(v) for v in t.tolist())
+        k = int(n.item())
+        flops = 6.0 * k * d * F
+        tf = flops / (t_ffn * 1e-3) / 1e12
+        rows[str(m)] = {"n_sel": k, "select_ms": round(t_sel, 4), "ffn_ms": round(t_ffn, 4),
+                        "tokens_per_s": round(world * L / (t_tot * 1e-3)),
+                        "ffn_tflops": round(tf, 1), "ffn_frac_bf16_peak": round(tf / bf16_peak, 4)}
+    res = {"metric": "sparse-prefill tokens/s", "unit": "tokens/s",
+           "workload": "token-selective-prefill: L 16384, d_model 5120, d_ff 25600, SwiGLU bf16, recent_n 128, "
+                       "min_keep 1, Y_attn rows scaled by exp(N(0,1))",
+           "value": rows["0.2"]["tokens_per_s"], "by_mass": rows,
+           "speedup_vs_dense": round(rows["0.2"]["tokens_per_s"] / rows["1.0"]["tokens_per_s"], 3),
+           "roofline": {"bound": "tensor", "kernel": "sffn_prefill FFN (tcgen05 SwiGLU + down GEMMs), mass 0.5",
+                        "achieved": rows["0.5"]["ffn_tflops"], "peak": bf16_peak, "unit": "TFLOP/s",
+                        "frac": rows["0.5"]["ffn_frac_bf16_peak"], "peak_source": peak_src,
+                        "flops_per_launch": 6.0 * rows["0.5"]["n_sel"] * d * F,
+                        "traffic": traffic_for("prefill_m05")}}
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = prefill_cpu_baseline(layer, X, Ya)
+    return res
+
+
+def prefill_cpu_baseline(layer_dev, X, Ya, nrows=8):
+    import numpy as np
+
+    import oracle as O
+    from tests.oracle_io import ffn_from_layer, mat_from_act
+    layer = {k: (v.cpu() if hasattr(v, "cpu") else v) for k, v in layer_dev.items()}
+    Xc, Yc = X.cpu(), Ya.cpu()
+    L = Xc.shape[0]
+    mask = np.ones(L, np.uint8)
+    rows = np.arange(0, L, L // nrows, dtype=np.int32)[:nrows]
+    nth = min(os.cpu_count() or 1, nrows)
+    t0 = time.perf_counter()
+    O.prefill_rows(ffn_from_layer(layer), mat_from_act(Xc), mat_from_act(Yc), mask, rows, nthreads=nth)
+    dt = time.perf_counter() - t0
+    return {"value": round(nrows / dt, 3), "unit": "selected rows/s", "cores": nth, "kind": "oracle",
+            "sample": f"{nrows} selected rows of the prefill FFN, fp64 oracle, {nth} threads"}
 
 
 def cpu_baseline(layer_dev, x_cpu, nthreads=None):
@@ -336,6 +454,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=1024)
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--prefill-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
