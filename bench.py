@@ -280,6 +280,17 @@ def run_ours(args):
     return res
 
 
+def run_prefill_only(args):
+    import torch
+
+    import __graft_entry__ as G
+    G.build()
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    res = bench_prefill(args, torch.device("cuda", local), rank, 1, None)
+    return {"prefill": res} if rank == 0 else None
+
+
 def traffic_for(key):
     """DRAM bytes per launch from a committed ncu capture, or None if the kernel
     sources changed since it was taken (profiles/traffic.json holds the hash)."""
@@ -455,11 +466,17 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="run only the prefill leg (profiling)")
     ap.add_argument("--prefill-steps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.impl == "reference":
+        res = run_reference(args)
+    elif args.no_decode:
+        res = run_prefill_only(args)
+    else:
+        res = run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 
