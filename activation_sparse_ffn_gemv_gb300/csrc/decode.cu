@@ -37,7 +37,11 @@ struct WF32 {
         f[2] = __uint_as_float(v.z);
         f[3] = __uint_as_float(v.w);
     }
-    static SFFN_DEV float load_x(const void *x, size_t i) { return static_cast<const float *>(x)[i]; }
+    static constexpr bool Q = false;  // no group scales
+    static SFFN_DEV float scale_at(const unsigned char *, uint32_t) { return 1.f; }
+    static SFFN_DEV void dequant(const uint4 &v, float, float *f) { unpack(v, f); }
+    // x elements matching weight unit u (x stored in its own dtype, 16-byte units)
+    static SFFN_DEV void load_xu(const uint4 *xrow, uint32_t u, float *f) { unpack(xrow[u], f); }
 };
 
 struct WBF16 {
@@ -49,8 +53,36 @@ struct WBF16 {
         f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
         f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
     }
-    static SFFN_DEV float load_x(const void *x, size_t i) {
-        return __bfloat162float(static_cast<const __nv_bfloat16 *>(x)[i]);
+    static constexpr bool Q = false;
+    static SFFN_DEV float scale_at(const unsigned char *, uint32_t) { return 1.f; }
+    static SFFN_DEV void dequant(const uint4 &v, float, float *f) { unpack(v, f); }
+    static SFFN_DEV void load_xu(const uint4 *xrow, uint32_t u, float *f) { unpack(xrow[u], f); }
+};
+
+// Symmetric int4 with one fp16 scale per 64 consecutive elements of a stored
+// row: a 16-byte unit holds 32 two's-complement codes (low nibble = even
+// column) and lies in group u / 2.  code * scale is exact in fp32, and so is its
+// product with a bf16 activation (at most 23 significant bits).
+struct WINT4 {
+    using X = __nv_bfloat16;
+    static constexpr int E = 32;
+    static constexpr bool Q = true;
+    static SFFN_DEV float scale_at(const unsigned char *srow, uint32_t u) {
+        return __half2float(*reinterpret_cast<const __half *>(srow + (u >> 1) * 2));
+    }
+    // nibble n (two's complement) -> n ^ 8 is the code + 8 as an unsigned value;
+    // OR-ing it into the mantissa of 2^23 gives 2^23 + code + 8 exactly
+    static SFFN_DEV void dequant(const uint4 &v, float s, float *f) {
+        const uint32_t w[4] = {v.x ^ 0x88888888u, v.y ^ 0x88888888u, v.z ^ 0x88888888u, v.w ^ 0x88888888u};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                f[8 * q + k] = (__uint_as_float(0x4B000000u | ((w[q] >> (4 * k)) & 0xFu)) - 8388616.0f) * s;
+    }
+    static SFFN_DEV void load_xu(const uint4 *xrow, uint32_t u, float *f) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) WBF16::unpack(xrow[4 * u + q], f + 8 * q);
     }
 };
 
@@ -113,17 +145,18 @@ SFFN_DEV void stage_x(float *xs, const void *x, int nb, int NBpad, int d) {
 // ---------------------------------------------------------------------------
 
 template <class W>
-__global__ void __launch_bounds__(256) k_down_norms(const void *wdT, int d, int F, float *norms) {
+__global__ void __launch_bounds__(256) k_down_norms(const void *wdT, const void *sdT, int d, int F, float *norms) {
     griddep_wait();
     const int lane = threadIdx.x & 31;
     const int j = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (j >= F) return;
     const int units = d / W::E;  // 16-byte units per stored row
     const char *row = static_cast<const char *>(wdT) + (size_t)j * (size_t)units * 16;
+    const unsigned char *srow = W::Q ? static_cast<const unsigned char *>(sdT) + (size_t)j * (d / 64) * 2 : nullptr;
     float acc = 0.f;
     for (int u = lane; u < units; u += 32) {
         float f[W::E];
-        W::unpack(ldg_stream(row + (size_t)u * 16), f);
+        W::dequant(ldg_stream(row + (size_t)u * 16), W::Q ? W::scale_at(srow, u) : 1.f, f);
 #pragma unroll
         for (int e = 0; e < W::E; ++e) acc = fmaf(f[e], f[e], acc);
     }
@@ -163,6 +196,7 @@ struct GateArgs {
     int32_t *err;
     const void *wdT;      // decide: down projection, read for this chunk's active rows
     float *part;          // decide: [C, nb, d] this CTA's fp32 partial of the output
+    const void *sg, *su, *sd;  // int4: fp16 group scales [F, d/64] of gate, up, down
 };
 
 constexpr int kGateWarps = 8;           // each warp streams its own rows
@@ -175,12 +209,15 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     const int d = a.d, F = a.F;
     const uint32_t units = (uint32_t)(d / W::E);  // 16-byte units per row
     const uint32_t row_bytes = units * 16u;
-    const uint32_t stage_bytes = UP ? 2u * row_bytes : row_bytes;
+    const uint32_t sbytes = W::Q ? (uint32_t)(d / 64) * 2u : 0u;  // group scales of one row
+    const uint32_t rspace = row_bytes + sbytes;    // a row (codes, then scales) in shared memory
+    const uint32_t stage_bytes = UP ? 2u * rspace : rspace;
+    const uint32_t xunits = (uint32_t)(d * (int)sizeof(typename W::X) / 16);
     const int D = a.stages;                        // stages (rows in flight) per warp
     unsigned char *ring = smraw;                   // [warps][D] stages
     unsigned char *xraw = smraw + (size_t)kGateWarps * D * stage_bytes;
     const uint4 *xs = reinterpret_cast<const uint4 *>(xraw);   // x in its own dtype [NB][d]
-    uint64_t *full = reinterpret_cast<uint64_t *>(xraw + (size_t)NB * row_bytes);  // [warps][D]
+    uint64_t *full = reinterpret_cast<uint64_t *>(xraw + (size_t)NB * xunits * 16);  // [warps][D]
     uint64_t *dbar = full + (size_t)kGateWarps * D;  // active-row copies after the stream
     __shared__ uint8_t sflag[kMaxChunk];
     __shared__ float sh[kMaxChunk][NB];
@@ -197,7 +234,19 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     unsigned char *wring = ring + (size_t)warp * D * stage_bytes;
     const char *gbase = static_cast<const char *>(a.wg) + (size_t)row0 * row_bytes;
     const char *ubase = UP ? static_cast<const char *>(a.wu) + (size_t)row0 * row_bytes : nullptr;
+    const char *gsbase = W::Q ? static_cast<const char *>(a.sg) + (size_t)row0 * sbytes : nullptr;
+    const char *usbase = W::Q && UP ? static_cast<const char *>(a.su) + (size_t)row0 * sbytes : nullptr;
     uint64_t pol = 0;
+    // one stage: gate row codes [+ scales] [+ up row codes [+ scales]]
+    auto issue_row = [&](unsigned char *stage, size_t r, uint64_t *bar) {
+        mbar_arrive_expect_tx(bar, stage_bytes);
+        bulk_load(stage, gbase + r * row_bytes, row_bytes, bar, pol);
+        if (W::Q) bulk_load(stage + row_bytes, gsbase + r * sbytes, sbytes, bar, pol);
+        if (UP) {
+            bulk_load(stage + rspace, ubase + r * row_bytes, row_bytes, bar, pol);
+            if (W::Q) bulk_load(stage + rspace + row_bytes, usbase + r * sbytes, sbytes, bar, pol);
+        }
+    };
     // Each warp keeps its own D row copies in flight (1-D bulk copies issued by
     // its lane 0) and re-issues into a stage as soon as it has consumed it: no
     // producer warp, so a slow warp never holds back another warp's stream.
@@ -206,12 +255,8 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
         for (int i = 0; i < D; ++i) mbar_init(&wfull[i], 1);
         mbar_fence_init();
         pol = l2_evict_first_policy();
-        for (int i = 0; i < D && i < nmine; ++i) {
-            const size_t r = (size_t)(warp + i * kGateWarps);
-            mbar_arrive_expect_tx(&wfull[i], stage_bytes);
-            bulk_load(wring + (size_t)i * stage_bytes, gbase + r * row_bytes, row_bytes, &wfull[i], pol);
-            if (UP) bulk_load(wring + (size_t)i * stage_bytes + row_bytes, ubase + r * row_bytes, row_bytes, &wfull[i], pol);
-        }
+        for (int i = 0; i < D && i < nmine; ++i)
+            issue_row(wring + (size_t)i * stage_bytes, (size_t)(warp + i * kGateWarps), &wfull[i]);
     }
     if (tid == 0) {
         s_abort = 0;
@@ -237,7 +282,8 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
         // This lane always handles units lane, lane + 32, ... of a row: for one
         // token its slice of x is unpacked into registers once and reused for
         // every row.  Units per lane <= UPL (d_model <= 4096).
-        constexpr int UPL = W::E == 8 ? 16 : 32;
+        constexpr int UPL = 128 / W::E;        // units per lane at d_model <= 4096
+        constexpr int CU = W::E >= 32 ? 1 : 4;  // units loaded together (ILP)
         constexpr bool XREG = NB == 1;
         float xr[XREG ? UPL * W::E : 1];
         if (XREG) {
@@ -245,7 +291,12 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
             for (int i = 0; i < UPL; ++i) {
                 const uint32_t u = i * 32 + lane;
                 float f[W::E];
-                W::unpack(u < units ? xs[u] : make_uint4(0, 0, 0, 0), f);
+                if (u < units) {
+                    W::load_xu(xs, u, f);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < W::E; ++e) f[e] = 0.f;
+                }
 #pragma unroll
                 for (int e = 0; e < W::E; ++e) xr[(XREG ? i * W::E + e : 0)] = f[e];
             }
@@ -276,49 +327,53 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) accg[b][c] = accu[b][c] = 0.f;
 #pragma unroll
-                for (int i0 = 0; i0 < UPL; i0 += 4) {
-                    uint4 vg[4], vu[4];
+                for (int i0 = 0; i0 < UPL; i0 += CU) {
+                    uint4 vg[CU], vu[CU];
+                    float scg[CU], scu[CU];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < CU; ++c) {
                         const uint32_t u = (i0 + c) * 32 + lane;
-                        vg[c] = u < units ? *reinterpret_cast<const uint4 *>(st + u * 16) : make_uint4(0, 0, 0, 0);
-                        if (UP)
-                            vu[c] = u < units ? *reinterpret_cast<const uint4 *>(st + row_bytes + u * 16)
-                                              : make_uint4(0, 0, 0, 0);
+                        const bool in = u < units;
+                        vg[c] = in ? *reinterpret_cast<const uint4 *>(st + u * 16) : make_uint4(0, 0, 0, 0);
+                        scg[c] = W::Q && in ? W::scale_at(st + row_bytes, u) : 1.f;
+                        if (UP) {
+                            vu[c] = in ? *reinterpret_cast<const uint4 *>(st + rspace + u * 16) : make_uint4(0, 0, 0, 0);
+                            scu[c] = W::Q && in ? W::scale_at(st + rspace + row_bytes, u) : 1.f;
+                        }
                     }
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < CU; ++c) {
                         const uint32_t u = (i0 + c) * 32 + lane;
                         float fg[W::E], fu[W::E];
-                        W::unpack(vg[c], fg);
-                        if (UP) W::unpack(vu[c], fu);
+                        W::dequant(vg[c], scg[c], fg);
+                        if (UP) W::dequant(vu[c], scu[c], fu);
 #pragma unroll
                         for (int b = 0; b < NB; ++b) {
                             float xf[W::E];
                             if (XREG) {
 #pragma unroll
                                 for (int e = 0; e < W::E; ++e) xf[e] = xr[XREG ? (i0 + c) * W::E + e : 0];
+                            } else if (u < units) {
+                                W::load_xu(xs + (size_t)b * xunits, u, xf);
                             } else {
-                                W::unpack(u < units ? xs[(size_t)b * units + u] : make_uint4(0, 0, 0, 0), xf);
+#pragma unroll
+                                for (int e = 0; e < W::E; ++e) xf[e] = 0.f;
                             }
 #pragma unroll
                             for (int e = 0; e < W::E; ++e) {
-                                accg[b][c] = fmaf(fg[e], xf[e], accg[b][c]);
-                                if (UP) accu[b][c] = fmaf(fu[e], xf[e], accu[b][c]);
+                                const int ai = CU == 1 ? (e & 3) : c;
+                                accg[b][ai] = fmaf(fg[e], xf[e], accg[b][ai]);
+                                if (UP) accu[b][ai] = fmaf(fu[e], xf[e], accu[b][ai]);
                             }
                         }
                     }
-                    if ((i0 + 4) * 32 >= (int)units) break;
+                    if ((i0 + CU) * 32 >= (int)units) break;
                 }
                 // stage consumed: refill it with this warp's row k + D
                 __syncwarp();
                 if (lane == 0 && k + D < nmine) {
                     fence_proxy_async_smem();
-                    const size_t rn = (size_t)(warp + (k + D) * kGateWarps);
-                    mbar_arrive_expect_tx(&wfull[si], stage_bytes);
-                    bulk_load(wring + (size_t)si * stage_bytes, gbase + rn * row_bytes, row_bytes, &wfull[si], pol);
-                    if (UP) bulk_load(wring + (size_t)si * stage_bytes + row_bytes, ubase + rn * row_bytes, row_bytes,
-                                      &wfull[si], pol);
+                    issue_row(wring + (size_t)si * stage_bytes, (size_t)(warp + (k + D) * kGateWarps), &wfull[si]);
                 }
                 float g = 0.f, uu = 0.f;
 #pragma unroll
@@ -350,6 +405,10 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
                 if (m != 0u && lane == 0) {
                     bulk_prefetch_l2(static_cast<const char *>(a.wdT) + (size_t)j * row_bytes, row_bytes);
                     if (!UP) bulk_prefetch_l2(static_cast<const char *>(a.wu) + (size_t)j * row_bytes, row_bytes);
+                    if (W::Q) {
+                        bulk_prefetch_l2(static_cast<const char *>(a.sd) + (size_t)j * sbytes, sbytes);
+                        if (!UP) bulk_prefetch_l2(static_cast<const char *>(a.su) + (size_t)j * sbytes, sbytes);
+                    }
                 }
                 // UP: h_j = a_j u_j now; otherwise the masked a_j, multiplied by u_j later
                 if (lane < NB) sh[r][lane] = active ? (UP ? av * uu : av) : 0.f;
@@ -388,9 +447,11 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     // the rows in ascending order (deterministic) into this CTA's partial.
     const int ndown = s_ndown;
     const int per_row_slots = UP ? 1 : 2;
-    const int cap = (int)((size_t)kGateWarps * D * stage_bytes / row_bytes) / per_row_slots;
+    const int cap = (int)((size_t)kGateWarps * D * stage_bytes / rspace) / per_row_slots;
     const char *wd = static_cast<const char *>(a.wdT);
     const char *wu = static_cast<const char *>(a.wu);
+    const char *sd = static_cast<const char *>(a.sd);
+    const char *suq = static_cast<const char *>(a.su);
     const int nwarps = blockDim.x >> 5;
     for (int b0 = 0, batch = 0;; b0 += cap, ++batch) {
         const int bn = min(cap, ndown - b0);
@@ -398,11 +459,17 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
             if (tid == 0) {
                 fence_proxy_async_smem();  // earlier generic reads of the ring precede the copies
                 const uint64_t pol = l2_evict_first_policy();
-                mbar_arrive_expect_tx(dbar, (uint32_t)(bn * per_row_slots) * row_bytes);
+                mbar_arrive_expect_tx(dbar, (uint32_t)(bn * per_row_slots) * rspace);
                 for (int i = 0; i < bn; ++i) {
                     const size_t j = (size_t)(row0 + sdown[b0 + i]);
-                    bulk_load(ring + (size_t)i * row_bytes, wd + j * row_bytes, row_bytes, dbar, pol);
-                    if (!UP) bulk_load(ring + (size_t)(cap + i) * row_bytes, wu + j * row_bytes, row_bytes, dbar, pol);
+                    unsigned char *dslot = ring + (size_t)i * rspace;
+                    bulk_load(dslot, wd + j * row_bytes, row_bytes, dbar, pol);
+                    if (W::Q) bulk_load(dslot + row_bytes, sd + j * sbytes, sbytes, dbar, pol);
+                    if (!UP) {
+                        unsigned char *uslot = ring + (size_t)(cap + i) * rspace;
+                        bulk_load(uslot, wu + j * row_bytes, row_bytes, dbar, pol);
+                        if (W::Q) bulk_load(uslot + row_bytes, suq + j * sbytes, sbytes, dbar, pol);
+                    }
                 }
             }
             const bool ok = mbar_wait(dbar, (uint32_t)batch & 1u);
@@ -411,36 +478,48 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
                 return;
             }
             if (!UP) {
-                constexpr int UPL = W::E == 8 ? 16 : 32;  // units per lane (d_model <= 4096)
+                constexpr int UPL = 128 / W::E;        // units per lane (d_model <= 4096)
+                constexpr int CU = W::E >= 32 ? 1 : 4;
                 for (int i = warp; i < bn; i += nwarps) {
-                    const unsigned char *ur = ring + (size_t)(cap + i) * row_bytes;
+                    const unsigned char *ur = ring + (size_t)(cap + i) * rspace;
                     float su[NB][4];
 #pragma unroll
                     for (int b = 0; b < NB; ++b)
 #pragma unroll
                         for (int c = 0; c < 4; ++c) su[b][c] = 0.f;
 #pragma unroll
-                    for (int i0 = 0; i0 < UPL; i0 += 4) {
-                        uint4 v[4];
+                    for (int i0 = 0; i0 < UPL; i0 += CU) {
+                        uint4 v[CU];
+                        float sc[CU];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < CU; ++c) {
                             const uint32_t u = (i0 + c) * 32 + lane;
-                            v[c] = u < units ? *reinterpret_cast<const uint4 *>(ur + u * 16) : make_uint4(0, 0, 0, 0);
+                            const bool in = u < units;
+                            v[c] = in ? *reinterpret_cast<const uint4 *>(ur + u * 16) : make_uint4(0, 0, 0, 0);
+                            sc[c] = W::Q && in ? W::scale_at(ur + row_bytes, u) : 1.f;
                         }
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < CU; ++c) {
                             const uint32_t u = (i0 + c) * 32 + lane;
                             float f[W::E];
-                            W::unpack(v[c], f);
+                            W::dequant(v[c], sc[c], f);
 #pragma unroll
                             for (int b = 0; b < NB; ++b) {
                                 float xf[W::E];
-                                W::unpack(u < units ? xs[(size_t)b * units + u] : make_uint4(0, 0, 0, 0), xf);
+                                if (u < units) {
+                                    W::load_xu(xs + (size_t)b * xunits, u, xf);
+                                } else {
 #pragma unroll
-                                for (int e = 0; e < W::E; ++e) su[b][c] = fmaf(f[e], xf[e], su[b][c]);
+                                    for (int e = 0; e < W::E; ++e) xf[e] = 0.f;
+                                }
+#pragma unroll
+                                for (int e = 0; e < W::E; ++e) {
+                                    const int ai = CU == 1 ? (e & 3) : c;
+                                    su[b][ai] = fmaf(f[e], xf[e], su[b][ai]);
+                                }
                             }
                         }
-                        if ((i0 + 4) * 32 >= (int)units) break;
+                        if ((i0 + CU) * 32 >= (int)units) break;
                     }
                     const int r = sdown[b0 + i];
 #pragma unroll
@@ -461,8 +540,9 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
                 for (int e = 0; e < W::E; ++e) acc[e] = 0.f;
                 for (int i = 0; i < bn; ++i) {
                     const float h = sh[sdown[b0 + i]][b];
+                    const unsigned char *dr = ring + (size_t)i * rspace;
                     float f[W::E];
-                    W::unpack(*reinterpret_cast<const uint4 *>(ring + (size_t)i * row_bytes + u * 16), f);
+                    W::dequant(*reinterpret_cast<const uint4 *>(dr + u * 16), W::Q ? W::scale_at(dr + row_bytes, u) : 1.f, f);
 #pragma unroll
                     for (int e = 0; e < W::E; ++e) acc[e] = fmaf(h, f[e], acc[e]);
                 }
@@ -1065,27 +1145,28 @@ DecodePlan make_decode_plan(int B, int d, int F) {
 }
 
 // Dynamic shared memory of the gate kernel with D rows in flight per warp.
-static size_t gate_smem(int NB, uint32_t row_bytes, uint32_t stage_bytes, int D) {
-    return (size_t)kGateWarps * D * stage_bytes + (size_t)NB * row_bytes +
-           sizeof(uint64_t) * ((size_t)kGateWarps * D + 1);
+static size_t gate_smem(size_t x_bytes, uint32_t stage_bytes, int D) {
+    return (size_t)kGateWarps * D * stage_bytes + x_bytes + sizeof(uint64_t) * ((size_t)kGateWarps * D + 1);
 }
 
 template <class W, int NB, bool UP>
 static cudaError_t launch_gate(const GateArgs &ga_in, const DecodePlan &p, cudaStream_t s) {
     GateArgs ga = ga_in;
     const uint32_t row_bytes = (uint32_t)(p.d / W::E) * 16u;
-    const uint32_t stage_bytes = (UP ? 2u : 1u) * row_bytes;
+    const uint32_t sbytes = W::Q ? (uint32_t)(p.d / 64) * 2u : 0u;
+    const uint32_t stage_bytes = (UP ? 2u : 1u) * (row_bytes + sbytes);
+    const size_t x_bytes = (size_t)NB * p.d * sizeof(typename W::X);
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, (const void *)k_gate<W, NB, UP>);
     if (e != cudaSuccess) return e;
-    const long avail = (long)device_smem_optin() - (long)fa.sharedSizeBytes - 1024 - (long)NB * row_bytes - 16;
+    const long avail = (long)device_smem_optin() - (long)fa.sharedSizeBytes - 1024 - (long)x_bytes - 16;
     long D = avail / ((long)kGateWarps * (stage_bytes + sizeof(uint64_t)));
     if (D > 4) D = 4;
     const int rows_per_warp = (p.R + kGateWarps - 1) / kGateWarps;
     if (D > rows_per_warp) D = rows_per_warp;
     if (D < 1) return cudaErrorInvalidConfiguration;
     ga.stages = (int)D;
-    const size_t smem = gate_smem(NB, row_bytes, stage_bytes, ga.stages);
+    const size_t smem = gate_smem(x_bytes, stage_bytes, ga.stages);
     e = set_max_smem((const void *)k_gate<W, NB, UP>, (int)smem);
     if (e != cudaSuccess) return e;
     return launch_k(k_gate<W, NB, UP>, dim3(p.C), dim3(kGateThreads), smem, s, ga);
@@ -1134,6 +1215,9 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     ga.err = err;
     ga.wdT = w->w_downT;
     ga.part = part;
+    ga.sg = w->s_gate;
+    ga.su = w->s_up;
+    ga.sd = w->s_downT;
     cudaError_t e = up ? launch_gate<W, NB, true>(ga, p, s) : launch_gate<W, NB, false>(ga, p, s);
     if (e != cudaSuccess || scores_only) return e;
 
@@ -1143,79 +1227,83 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
         nparts = p.C;
         list_ctas = true;
     }
-    bool have_h = up;  // keep-ratio: h_j known before the down pass
-    if (keep) {
-        KeepArgs ka = {};
-        ka.score = score;
-        ka.aeff = aeff;
-        ka.uval = up ? uval : nullptr;
-        ka.lh = up ? lh : nullptr;
-        ka.F = p.F;
-        double kk = floor((double)p.F * (double)c.param);
-        int k = kk < 1.0 ? 1 : (int)kk;
-        if (k > p.F) k = p.F;
-        ka.k = k;
-        ka.nb = p.nb;
-        ka.C = p.C;
-        ka.cnt = cnt;
-        ka.lidx = lidx;
-        ka.mask = p.nb > 1 ? mask : nullptr;
-        e = launch_k(k_keep_ratio, dim3(p.nb), dim3(kSelThreads), 0, s, ka);
-        if (e != cudaSuccess) return e;
-        if (p.nb > 1) {
-            e = launch_k(k_union, dim3(1), dim3(kSelThreads), 0, s, (const uint32_t *)mask, p.nb, p.F, p.C, cnt, lidx,
-                         (const float *)aeff, (const float *)uval, up ? lh : (float *)nullptr);
+    if constexpr (W::E <= 8) {  // keep-ratio paths: fp32 / bf16 weights
+        bool have_h = up;  // keep-ratio: h_j known before the down pass
+        if (keep) {
+            KeepArgs ka = {};
+            ka.score = score;
+            ka.aeff = aeff;
+            ka.uval = up ? uval : nullptr;
+            ka.lh = up ? lh : nullptr;
+            ka.F = p.F;
+            double kk = floor((double)p.F * (double)c.param);
+            int k = kk < 1.0 ? 1 : (int)kk;
+            if (k > p.F) k = p.F;
+            ka.k = k;
+            ka.nb = p.nb;
+            ka.C = p.C;
+            ka.cnt = cnt;
+            ka.lidx = lidx;
+            ka.mask = p.nb > 1 ? mask : nullptr;
+            e = launch_k(k_keep_ratio, dim3(p.nb), dim3(kSelThreads), 0, s, ka);
             if (e != cudaSuccess) return e;
+            if (p.nb > 1) {
+                e = launch_k(k_union, dim3(1), dim3(kSelThreads), 0, s, (const uint32_t *)mask, p.nb, p.F, p.C, cnt, lidx,
+                             (const float *)aeff, (const float *)uval, up ? lh : (float *)nullptr);
+                if (e != cudaSuccess) return e;
+            }
         }
-    }
 
-    const int threads = ((p.d / 8) + 31) / 32 * 32;
-    const int max_rows = (p.F + p.G2 - 1) / p.G2 + 1;
-    if (!keep) {
-        // nothing between the gate kernel and the reduction
-    } else if (have_h) {
-        DownArgs da = {};
-        da.wdT = w->w_downT;
-        da.d = p.d;
-        da.F = p.F;
-        da.nb = p.nb;
-        da.R = p.R;
-        da.C = p.C;
-        da.list_u = p.list_u;
-        da.cnt = cnt;
-        da.lidx = lidx;
-        da.lh = lh;
-        da.part = part;
-        da.active_idx = p.nb == 1 ? c.active_idx : nullptr;
-        da.n_active = p.nb == 1 ? c.n_active : nullptr;
-        da.by_chunk = 0;  // keep-ratio lists are one block, not per gate chunk
-        da.max_rows = max_rows;
-        const size_t smem = sizeof(int) * (kMaxC + 1 + da.max_rows) + sizeof(float) * (size_t)da.max_rows * NB;
-        e = set_max_smem((const void *)k_down<W, NB>, (int)smem);
-        if (e == cudaSuccess) e = launch_k(k_down<W, NB>, dim3(nparts), dim3(threads), smem, s, da);
+        const int threads = ((p.d / 8) + 31) / 32 * 32;
+        const int max_rows = (p.F + p.G2 - 1) / p.G2 + 1;
+        if (!keep) {
+            // nothing between the gate kernel and the reduction
+        } else if (have_h) {
+            DownArgs da = {};
+            da.wdT = w->w_downT;
+            da.d = p.d;
+            da.F = p.F;
+            da.nb = p.nb;
+            da.R = p.R;
+            da.C = p.C;
+            da.list_u = p.list_u;
+            da.cnt = cnt;
+            da.lidx = lidx;
+            da.lh = lh;
+            da.part = part;
+            da.active_idx = p.nb == 1 ? c.active_idx : nullptr;
+            da.n_active = p.nb == 1 ? c.n_active : nullptr;
+            da.by_chunk = 0;  // keep-ratio lists are one block, not per gate chunk
+            da.max_rows = max_rows;
+            const size_t smem = sizeof(int) * (kMaxC + 1 + da.max_rows) + sizeof(float) * (size_t)da.max_rows * NB;
+            e = set_max_smem((const void *)k_down<W, NB>, (int)smem);
+            if (e == cudaSuccess) e = launch_k(k_down<W, NB>, dim3(nparts), dim3(threads), smem, s, da);
+        } else {
+            UpDownArgs ua = {};
+            ua.wu = w->w_up;
+            ua.wdT = w->w_downT;
+            ua.x = c.x;
+            ua.d = p.d;
+            ua.F = p.F;
+            ua.nb = p.nb;
+            ua.R = p.R;
+            ua.C = p.C;
+            ua.list_u = p.list_u;
+            ua.cnt = cnt;
+            ua.lidx = lidx;
+            ua.aeff = aeff;
+            ua.uval = nullptr;
+            ua.part = part;
+            ua.active_idx = p.nb == 1 ? c.active_idx : nullptr;
+            ua.n_active = p.nb == 1 ? c.n_active : nullptr;
+            const size_t smem = sizeof(float) * NB * p.d + sizeof(int) * (kMaxC + 1 + max_rows);
+            e = set_max_smem((const void *)k_updown<W, NB, false>, (int)smem);
+            if (e == cudaSuccess) e = launch_k(k_updown<W, NB, false>, dim3(p.G2), dim3(threads), smem, s, ua);
+        }
+        if (e != cudaSuccess) return e;
     } else {
-        UpDownArgs ua = {};
-        ua.wu = w->w_up;
-        ua.wdT = w->w_downT;
-        ua.x = c.x;
-        ua.d = p.d;
-        ua.F = p.F;
-        ua.nb = p.nb;
-        ua.R = p.R;
-        ua.C = p.C;
-        ua.list_u = p.list_u;
-        ua.cnt = cnt;
-        ua.lidx = lidx;
-        ua.aeff = aeff;
-        ua.uval = nullptr;
-        ua.part = part;
-        ua.active_idx = p.nb == 1 ? c.active_idx : nullptr;
-        ua.n_active = p.nb == 1 ? c.n_active : nullptr;
-        const size_t smem = sizeof(float) * NB * p.d + sizeof(int) * (kMaxC + 1 + max_rows);
-        e = set_max_smem((const void *)k_updown<W, NB, false>, (int)smem);
-        if (e == cudaSuccess) e = launch_k(k_updown<W, NB, false>, dim3(p.G2), dim3(threads), smem, s, ua);
+        if (keep) return cudaErrorNotSupported;  // rejected by the API for int4
     }
-    if (e != cudaSuccess) return e;
 
     ReduceArgs ra = {};
     ra.part = part;
@@ -1250,6 +1338,7 @@ sffn_status run_decode(const DecodeCall &c, const DecodePlan &p, cudaStream_t s)
     switch (c.w->wdtype) {
     case SFFN_F32: e = launch_decode_w<WF32>(c, p, s); break;
     case SFFN_BF16: e = launch_decode_w<WBF16>(c, p, s); break;
+    case SFFN_INT4_G64: e = launch_decode_w<WINT4>(c, p, s); break;
     default: return SFFN_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? SFFN_OK : SFFN_ERR_CUDA;
@@ -1259,8 +1348,15 @@ sffn_status run_down_norms(const sffn_ffn_weights *w, float *norms, cudaStream_t
     cudaError_t e;
     const dim3 grid((w->d_ff + 7) / 8), block(256);
     switch (w->wdtype) {
-    case SFFN_F32: e = launch_k(k_down_norms<WF32>, grid, block, 0, s, w->w_downT, w->d_model, w->d_ff, norms); break;
-    case SFFN_BF16: e = launch_k(k_down_norms<WBF16>, grid, block, 0, s, w->w_downT, w->d_model, w->d_ff, norms); break;
+    case SFFN_F32:
+        e = launch_k(k_down_norms<WF32>, grid, block, 0, s, w->w_downT, (const void *)nullptr, w->d_model, w->d_ff, norms);
+        break;
+    case SFFN_BF16:
+        e = launch_k(k_down_norms<WBF16>, grid, block, 0, s, w->w_downT, (const void *)nullptr, w->d_model, w->d_ff, norms);
+        break;
+    case SFFN_INT4_G64:
+        e = launch_k(k_down_norms<WINT4>, grid, block, 0, s, w->w_downT, w->s_downT, w->d_model, w->d_ff, norms);
+        break;
     default: return SFFN_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? SFFN_OK : SFFN_ERR_CUDA;

@@ -44,7 +44,10 @@
  *  - Matrices are row-major.  The three weight matrices are stored neuron-major,
  *    each [d_ff, d_model]: w_gate[j,:], w_up[j,:] and w_downT[j,:] = W_down[:,j].
  *  - Shape limits: d_model % 8 == 0 (fp32/bf16), d_model % 64 == 0 (int4-g64),
- *    8 <= d_model <= 8192, 1 <= d_ff <= 65536, 1 <= B <= 8.
+ *    8 <= d_model <= 8192, 1 <= d_ff <= 65536, 1 <= B <= 8.  Decode also needs
+ *    d_model <= 4096, and for int4-g64 d_model % 512 == 0 (one row's scales are a
+ *    multiple of 16 bytes); int4-g64 decode supports the exact and threshold
+ *    rules (keep-ratio returns SFFN_ERR_UNSUPPORTED).
  */
 #ifndef SFFN_H
 #define SFFN_H

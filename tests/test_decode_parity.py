@@ -132,3 +132,53 @@ def test_config_qwen_keep_ratio_full(sffn, M):
     layer = W.make_ffn_layer(3, seed=0, layer=M)
     x = W.make_tokens(3, 1, seed=M)
     run_and_check_decode(sffn, layer, x, "keep_ratio", "gate_up", 1.0 / M, nthreads=16)
+
+
+# int4 group-quantised weights (symmetric codes, fp16 scale per 64 columns)
+
+def _tau_at(layer, x, q, score="gate"):
+    from tests.oracle_io import ffn_from_layer, mat_from_act
+    import oracle as O
+    ref = O.decode(ffn_from_layer(layer), mat_from_act(x), O.THRESHOLD,
+                   O.SCORE_GATE if score == "gate" else O.SCORE_GATE_UP, 0.0, details=True, nthreads=16)
+    return float(np.quantile(ref["score"], q))
+
+
+@pytest.mark.parametrize("case", [(512, 700, 1), (1024, 2050, 3), (512, 96, 8)], ids=lambda c: "-".join(map(str, c)))
+@pytest.mark.parametrize("score", ["gate", "gate_up"])
+def test_int4_threshold_small(sffn, case, score):
+    d, F, B = case
+    layer = W.make_ffn_layer(4, seed=31, d_model=d, d_ff=F)
+    x = W.make_tokens(4, B, seed=7, d_model=d)
+    tau = _tau_at(layer, x, 0.8, score)
+    r = run_and_check_decode(sffn, layer, x, "threshold", score, tau)
+    assert 0.1 < r["n_active"].mean() / F < 0.3
+
+
+def test_int4_exact_silu_is_dense(sffn):
+    # SiLU is almost never exactly 0: exact gating keeps (nearly) every neuron
+    d, F = 512, 300
+    layer = W.make_ffn_layer(4, seed=33, d_model=d, d_ff=F)
+    x = W.make_tokens(4, 2, seed=8, d_model=d)
+    r = run_and_check_decode(sffn, layer, x, "exact")
+    assert (r["n_active"] >= F - 2).all()
+
+
+@pytest.mark.parametrize("a", [0.1, 0.6])
+def test_config_qwen_int4_threshold_full(sffn, a):
+    layer = W.make_ffn_layer(4, seed=0, layer=int(a * 10))
+    x = W.make_tokens(4, 1, seed=int(a * 10))
+    tau = _tau_at(layer, x, 1.0 - a)
+    r = run_and_check_decode(sffn, layer, x, "threshold", "gate", tau, nthreads=16)
+    assert abs(r["n_active"].mean() / layer["d_ff"] - a) < 0.01
+
+
+def test_int4_keep_ratio_unsupported(sffn):
+    layer = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in
+             W.make_ffn_layer(4, seed=1, d_model=512, d_ff=128).items()}
+    w = sffn.Weights(layer)
+    w.set_down_norms(sffn.down_norms(w))
+    x = W.make_tokens(4, 1, d_model=512).cuda()
+    with pytest.raises(sffn.SffnError) as e:
+        sffn.decode(x, w, sffn.MODE_KEEP_RATIO, sffn.SCORE_GATE, 0.5)
+    assert e.value.status == sffn.ERR_UNSUPPORTED
