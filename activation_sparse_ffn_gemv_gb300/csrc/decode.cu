@@ -265,6 +265,9 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     }
     // x may be the previous layer's output: read it only after the dependency wait
     griddep_wait();
+    // the reduction may be scheduled now (its small CTAs fit beside this one);
+    // it waits for this grid's completion before reading the partials
+    griddep_launch_dependents();
     {
         constexpr int XE = 16 / (int)sizeof(typename W::X);
         const int per_row = d / XE, total = NB * per_row;
@@ -1161,7 +1164,7 @@ static cudaError_t launch_gate(const GateArgs &ga_in, const DecodePlan &p, cudaS
     if (e != cudaSuccess) return e;
     const long avail = (long)device_smem_optin() - (long)fa.sharedSizeBytes - 1024 - (long)x_bytes - 16;
     long D = avail / ((long)kGateWarps * (stage_bytes + sizeof(uint64_t)));
-    if (D > 4) D = 4;
+    if (D > 16) D = 16;  // small rows: a warp's whole share of the chunk can be in flight
     const int rows_per_warp = (p.R + kGateWarps - 1) / kGateWarps;
     if (D > rows_per_warp) D = rows_per_warp;
     if (D < 1) return cudaErrorInvalidConfiguration;

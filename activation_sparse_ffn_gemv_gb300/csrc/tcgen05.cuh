@@ -91,7 +91,7 @@ SFFN_DEV uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
 
 // Instruction descriptor for kind::f16: bf16 x bf16 -> fp32, M x N, A K-major,
 // B K-major or MN-major.
-constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_major) {
     return (1u << 4)                          // D format: f32
            | (1u << 7)                        // A format: bf16
            | (1u << 10)                       // B format: bf16

@@ -274,6 +274,10 @@ def run_ours(args):
         pf = bench_prefill(args, dev, rank, world, dist)
         if rank == 0:
             res["prefill"] = pf
+    if not args.no_sweeps:
+        sw = bench_decode_sweeps(args, dev)
+        if rank == 0:
+            res["decode_configs"] = sw
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -289,6 +293,136 @@ def run_prefill_only(args):
     torch.cuda.set_device(local)
     res = bench_prefill(args, torch.device("cuda", local), rank, 1, None)
     return {"prefill": res} if rank == 0 else None
+
+
+def _time_graph(enqueue, stream, steps, warmup):
+    """Capture enqueue() in a CUDA graph; device ms per replay."""
+    import torch
+    with torch.cuda.stream(stream):
+        enqueue()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        enqueue()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def bench_decode_sweeps(args, dev, T=256):
+    """The other decode workloads: int4 active-fraction sweep with breakeven,
+    keep-ratio tiers, batched tokens, the tiny fp32 layer.  Each point is a
+    CUDA graph of T single-call decodes rotating over the workload's layers."""
+    import numpy as np
+    import torch
+
+    from activation_sparse_ffn_gemv_gb300 import sffn
+    from activation_sparse_ffn_gemv_gb300 import workloads as W
+    stream = torch.cuda.Stream(device=dev)
+    hbm = peaks()[0]
+    out = {}
+
+    def rowb(c):
+        d = c["d_model"]
+        return {"f32": 4.0 * d, "bf16": 2.0 * d, "int4_g64": d / 2 + 2.0 * d / 64}[c["wdtype"]]
+
+    def run_points(cfgn, nl, points, B=1):
+        """points: list of (mode, score, param_per_layer); returns us/token, mean active fraction."""
+        c = W.CONFIGS[cfgn]
+        layers = [W.make_ffn_layer(cfgn, seed=100, layer=l, device=dev) for l in range(nl)]
+        ws = [sffn.Weights(L) for L in layers]
+        for w in ws:
+            w.set_down_norms(sffn.down_norms(w))
+        x = W.make_tokens(cfgn, T * B, seed=5, device=dev)
+        F = c["d_ff"]
+        o = torch.empty_like(x)
+        idx = torch.empty((T * B, F), dtype=torch.int32, device=dev)
+        n = torch.empty(T * B, dtype=torch.int32, device=dev)
+        work = sffn.alloc_workspace(sffn.WS_DECODE, B, ws[0], dev)
+        res = []
+        for mode, score, params in points:
+            def enq():
+                for t in range(T):
+                    sl = slice(t * B, (t + 1) * B)
+                    sffn.decode(x[sl], ws[t % nl], mode, score, params[t % nl], out=o[sl], active_idx=idx[sl],
+                                n_active=n[sl], workspace=work, stream=stream)
+            ms = _time_graph(enq, stream, max(3, args.steps // 3), args.warmup)
+            res.append((ms * 1e3 / (T * B), float(n.float().mean().item()) / F))
+        return c, layers, ws, x, res
+
+    # int4 sweep: threshold tau_a = (1 - a) quantile of the layer's gate scores
+    c = W.CONFIGS[4]
+    nl = c["layers"]
+    layers = [W.make_ffn_layer(4, seed=100, layer=l, device=dev) for l in range(nl)]
+    ws = [sffn.Weights(L) for L in layers]
+    for w in ws:
+        w.set_down_norms(sffn.down_norms(w))
+    calib = W.make_tokens(4, 256, seed=77, device=dev)
+    sc_ws = sffn.alloc_workspace(sffn.WS_DECODE, 8, ws[0], dev)
+    taus = {}
+    for l, w in enumerate(ws):
+        sc = torch.cat([sffn.gate_scores(calib[i:i + 8], w, sffn.SCORE_GATE, workspace=sc_ws) for i in range(0, 256, 8)])
+        q = torch.quantile(sc.flatten()[::4].float(), torch.tensor([1.0 - a for a in c["sweep_a"]], device=dev))
+        taus[l] = q.tolist()
+    del layers, ws, sc_ws
+    pts = [(sffn.MODE_THRESHOLD, sffn.SCORE_GATE, [taus[l][i] if c["sweep_a"][i] < 1.0 else 0.0 for l in range(nl)])
+           for i in range(len(c["sweep_a"]))]
+    pts.append((sffn.MODE_THRESHOLD, sffn.SCORE_GATE, [0.0] * nl))  # dense: tau = 0 keeps all
+    cfg, _, _, _, res = run_points(4, nl, pts)
+    dense_us = res[-1][0]
+    r = rowb(cfg)
+    F = cfg["d_ff"]
+    sweep = []
+    for (a_t, (us, a)) in zip(cfg["sweep_a"], res[:-1]):
+        b = F * r * (1 + 2 * a)
+        sweep.append({"a_target": a_t, "a": round(a, 4), "us_per_token": round(us, 3),
+                      "gbps": round(b / (us * 1e-6) / 1e9, 1), "frac_hbm": round(b / (us * 1e-6) / 1e9 / hbm, 4),
+                      "speedup_vs_dense": round(dense_us / us, 3)})
+    be = None
+    for p0, p1 in zip(sweep, sweep[1:]):
+        if p0["us_per_token"] <= dense_us <= p1["us_per_token"]:
+            be = p0["a"] + (dense_us - p0["us_per_token"]) * (p1["a"] - p0["a"]) / (
+                p1["us_per_token"] - p0["us_per_token"])
+    out["int4_threshold_sweep"] = {"workload": "qwen2.5-3b-swiglu-int4g64: d_model 2048, d_ff 11008, 36 layers, "
+                                               "threshold on |SiLU(g)|*||W_down[:,j]||, B=1",
+                                   "dense_us_per_token": round(dense_us, 3), "points": sweep,
+                                   "breakeven_active_fraction": None if be is None else round(be, 3)}
+    torch.cuda.empty_cache()
+
+    # keep-ratio tiers (gate-and-up score)
+    M = W.CONFIGS[3]["keep_M"]
+    cfg, _, _, _, res = run_points(3, W.CONFIGS[3]["layers"],
+                                   [(sffn.MODE_KEEP_RATIO, sffn.SCORE_GATE_UP, [1.0 / m] * 36) for m in M])
+    r = rowb(cfg)
+    F = cfg["d_ff"]
+    out["keep_ratio"] = {"workload": "qwen2.5-3b-swiglu: d_model 2048, d_ff 11008 bf16, 36 layers, "
+                                     "score |SiLU(g)*u|*||W_down[:,j]||, B=1",
+                         "by_M": {str(m): {"us_per_token": round(us, 3), "a": round(a, 4),
+                                           "gbps": round(F * r * (2 + a) / (us * 1e-6) / 1e9, 1)}
+                                  for m, (us, a) in zip(M, res)}}
+    torch.cuda.empty_cache()
+
+    # batched tokens on the Llama shape (union of active rows read once)
+    bt = {}
+    for B in (4, 8):
+        cfg, _, _, _, res = run_points(2, 8, [(sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0] * 8)], B=B)
+        bt[str(B)] = {"us_per_token": round(res[0][0], 3), "a_per_token": round(res[0][1], 4)}
+        torch.cuda.empty_cache()
+    out["batched_exact_llama"] = bt
+
+    # tiny fp32 ReGLU layer (L2 resident, launch bound: us/token only)
+    cfg, _, _, _, res = run_points(1, 1, [(sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0])])
+    out["tiny_fp32"] = {"us_per_token": round(res[0][0], 3), "a": round(res[0][1], 4)}
+    return out
 
 
 def traffic_for(key):
@@ -466,6 +600,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-sweeps", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="run only the prefill leg (profiling)")
     ap.add_argument("--prefill-steps", type=int, default=10)
     args = ap.parse_args()
