@@ -197,6 +197,12 @@ struct GateArgs {
     const void *wdT;      // decide: down projection, read for this chunk's active rows
     float *part;          // decide: [C, nb, d] this CTA's fp32 partial of the output
     const void *sg, *su, *sd;  // int4: fp16 group scales [F, d/64] of gate, up, down
+    // fused final reduction (all CTAs co-resident): grid barrier words in the
+    // workspace, the output and the per-token index lists
+    unsigned *gbar;            // [2]: arrivals, phase (zero before first use; self-resetting)
+    void *out;
+    int out_f32;
+    int32_t *active_idx, *n_active;
 };
 
 constexpr int kGateWarps = 8;           // each warp streams its own rows
@@ -420,7 +426,10 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
         }
     }
     __syncthreads();
-    if (!a.decide || s_abort) return;
+    // after a timed-out copy the CTA still meets the grid barrier (so that the
+    // barrier words stay consistent) but streams nothing more
+    if (!a.decide || (s_abort && !a.gbar)) return;
+    bool failed = s_abort;
 
     // ordered compaction of this chunk: one list per token for the active_idx
     // output, and (in shared memory) the chunk's rows active for any token
@@ -448,7 +457,7 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     // in one round trip; a warp per row forms u_j and h_j = a_j u_j; then every
     // thread owns 16-byte column units and accumulates h_j * W_down[:, j] over
     // the rows in ascending order (deterministic) into this CTA's partial.
-    const int ndown = s_ndown;
+    const int ndown = failed ? 0 : s_ndown;
     const int per_row_slots = UP ? 1 : 2;
     const int cap = (int)((size_t)kGateWarps * D * stage_bytes / rspace) / per_row_slots;
     const char *wd = static_cast<const char *>(a.wdT);
@@ -478,7 +487,8 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
             const bool ok = mbar_wait(dbar, (uint32_t)batch & 1u);
             if (!__syncthreads_and(ok)) {
                 if (tid == 0) record_error(a.err, SFFN_ERR_TIMEOUT);
-                return;
+                failed = true;
+                break;
             }
             if (!UP) {
                 constexpr int UPL = 128 / W::E;        // units per lane (d_model <= 4096)
@@ -563,6 +573,83 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
         }
         if (b0 + cap >= ndown) break;
         __syncthreads();  // the next batch overwrites the ring
+    }
+    if (!a.gbar) return;
+
+    // ---- grid barrier: every CTA's partial and chunk counts are written ----
+    // One CTA per SM and grid <= #SMs, so all CTAs are resident; the wait is
+    // bounded all the same.  gbar[0] counts arrivals and is back at 0 when the
+    // barrier opens; gbar[1] is the phase the last arrival advances.
+    __shared__ int s_bar_ok;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        volatile unsigned *vphase = a.gbar + 1;
+        const unsigned phase = *vphase;
+        __threadfence();  // the phase is read before this CTA's arrival counts
+        int ok = 1;
+        if (atomicAdd(a.gbar, 1u) == gridDim.x - 1) {
+            atomicExch(a.gbar, 0u);
+            __threadfence();
+            atomicExch(a.gbar + 1, phase + 1u);
+        } else {
+            const uint64_t t0 = globaltimer_ns();
+            while (*vphase == phase)
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    ok = 0;
+                    record_error(a.err, SFFN_ERR_TIMEOUT);
+                    break;
+                }
+        }
+        __threadfence();
+        s_bar_ok = ok;
+    }
+    __syncthreads();
+    if (!s_bar_ok || failed) return;
+
+    // ---- output columns: blocks of 32, sums over the C partials in a fixed order
+    {
+        float *red = &sh[0][0];  // [8][32] (sh holds >= 256 floats and is free now)
+        const int lane32 = tid & 31, grp = tid >> 5;   // 8 groups of 32 threads
+        const size_t total = (size_t)a.nb * d;
+        const int C = gridDim.x;
+        for (size_t cb = (size_t)blockIdx.x * 32; cb < total; cb += (size_t)C * 32) {
+            const size_t col = cb + lane32;
+            float sum = 0.f;
+            if (col < total) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int pp = grp + 8 * i;
+                    v[i] = pp < C ? __ldcg(a.part + (size_t)pp * total + col) : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) sum += v[i];
+                for (int pp = grp + 256; pp < C; pp += 8) sum += __ldcg(a.part + (size_t)pp * total + col);
+            }
+            red[grp * 32 + lane32] = sum;
+            __syncthreads();
+            if (grp == 0 && col < total) {
+                float t = red[lane32];
+#pragma unroll
+                for (int g2 = 1; g2 < 8; ++g2) t += red[g2 * 32 + lane32];
+                if (a.out_f32) static_cast<float *>(a.out)[col] = t;
+                else static_cast<uint16_t *>(a.out)[col] = f32_to_bf16_bits(t);
+            }
+            __syncthreads();
+        }
+    }
+    // ---- this chunk's ascending index lists at their global positions
+    for (int b = 0; b < a.nb; ++b) {
+        const int *cnt = a.cnt + (size_t)b * a.C;
+        int sacc = 0;
+        for (int c = tid; c < (int)blockIdx.x; c += blockDim.x) sacc += __ldcg(cnt + c);
+        int off;
+        block_excl_scan(sacc, scan_tmp, &off);
+        const int mine = __ldcg(cnt + blockIdx.x);
+        for (int i = tid; i < mine; i += blockDim.x)
+            a.active_idx[(size_t)b * F + off + i] = __ldcg(a.lidx + (size_t)b * F + row0 + i);
+        if (blockIdx.x == gridDim.x - 1 && tid == 0) a.n_active[b] = off + mine;
     }
 }
 
@@ -1062,8 +1149,16 @@ __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
         const size_t c = (size_t)blockIdx.x * 32 + lane;
         float s = 0.f;
         if (c < total) {
-#pragma unroll 8
-            for (int p = grp; p < a.G2; p += 8) s += a.part[(size_t)p * total + c];
+            // every load in flight at once (G2 <= 8 * 32); summed in a fixed order
+            float v[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int p = grp + 8 * i;
+                v[i] = p < a.G2 ? a.part[(size_t)p * total + c] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) s += v[i];
+            for (int p = grp + 256; p < a.G2; p += 8) s += a.part[(size_t)p * total + c];
         }
         red[grp][lane] = s;
         __syncthreads();
@@ -1134,7 +1229,10 @@ DecodePlan make_decode_plan(int B, int d, int F) {
     p.nlists = B + (B > 1 ? 1 : 0);
     p.list_u = B > 1 ? B : 0;
     size_t o = 0;
-    p.off_err = o; o = align_up(o + sizeof(int32_t));
+    // control block: error word, then the gate kernel's grid-barrier words
+    p.off_err = o;
+    p.off_bar = o + sizeof(int32_t);
+    o = align_up(o + sizeof(int32_t) + 2 * sizeof(unsigned));
     p.off_cnt = o; o = align_up(o + sizeof(int) * (size_t)p.nlists * p.C);
     p.off_lidx = o; o = align_up(o + sizeof(int) * (size_t)p.nlists * F);
     p.off_lh = o; o = align_up(o + sizeof(float) * (size_t)B * F);
@@ -1216,13 +1314,21 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     ga.lidx = lidx;
     ga.lh = lh;
     ga.err = err;
+    // exact / threshold with every gate CTA resident: the gate kernel finishes
+    // the call itself (grid barrier + distributed reduction + index lists)
+    const bool fused = !scores_only && !keep && p.C <= device_sm_count();
+    ga.gbar = fused ? reinterpret_cast<unsigned *>(ws + p.off_bar) : nullptr;
+    ga.out = c.out;
+    ga.out_f32 = w->wdtype == SFFN_F32;
+    ga.active_idx = c.active_idx;
+    ga.n_active = c.n_active;
     ga.wdT = w->w_downT;
     ga.part = part;
     ga.sg = w->s_gate;
     ga.su = w->s_up;
     ga.sd = w->s_downT;
     cudaError_t e = up ? launch_gate<W, NB, true>(ga, p, s) : launch_gate<W, NB, false>(ga, p, s);
-    if (e != cudaSuccess || scores_only) return e;
+    if (e != cudaSuccess || scores_only || fused) return e;
 
     int nparts = p.G2;
     bool list_ctas = p.nb > 1;

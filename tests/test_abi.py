@@ -124,4 +124,42 @@ def test_workspace_checks_on_gpu(S):
                        ws.data_ptr(), need, None)
     assert st == S.OK
     torch.cuda.synchronize()
+    # control block: the barrier's arrival count is back at zero after the call
+    # and its phase word has advanced once per call
+    ctl = ws[:12].cpu().view(torch.int32).tolist()
+    assert ctl[0] == 0 and ctl[1] == 0 and ctl[2] >= 1
+    for _ in range(3):
+        assert L.sffn_decode(x.data_ptr(), 1, w.ref(), 0, 0, 0.0, out.data_ptr(), idx.data_ptr(), n.data_ptr(),
+                             ws.data_ptr(), need, None) == S.OK
+    torch.cuda.synchronize()
+    ctl2 = ws[:12].cpu().view(torch.int32).tolist()
+    assert ctl2[1] == 0 and ctl2[2] == ctl[2] + 3
+    assert S.read_device_error(ws) == 0
+    assert ws[:12].cpu().view(torch.int32).tolist() == [0, 0, 0]
+
+
+@pytest.mark.gpu
+def test_workspace_shared_between_entry_points(S):
+    # one buffer serves token selection, prefill and decode in turn: the
+    # control block stays valid whichever call used the buffer last
+    from activation_sparse_ffn_gemv_gb300 import workloads as W
+    d, F, L = 256, 512, 300
+    layer = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in
+             W.make_ffn_layer(5, seed=2, d_model=d, d_ff=F).items()}
+    w = S.Weights(layer)
+    need = max(S.workspace_size(S.WS_DECODE, 8, w), S.workspace_size(S.WS_SELECT, L, w),
+               S.workspace_size(S.WS_PREFILL, L, w))
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    X, Ya = (t.cuda() for t in W.make_prefill_inputs(L, d, seed=3))
+    xt = W.make_tokens(5, 8, seed=4, d_model=d).cuda()
+    ref_out, ref_idx, ref_n = S.decode(xt, w, S.MODE_EXACT)
+    for _ in range(2):
+        sel, n = S.token_select(Ya, 0.5, 16, 1, workspace=ws)
+        S.prefill(X, Ya, w, sel, n, workspace=ws)
+        o, i, nn = S.decode(xt, w, S.MODE_EXACT, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(o, ref_out) and torch.equal(nn, ref_n)
+        for b in range(8):
+            k = int(nn[b])
+            assert torch.equal(i[b, :k], ref_idx[b, :k])
     assert S.read_device_error(ws) == 0
