@@ -252,8 +252,9 @@ sffn_status sffn_read_device_error(void *workspace, int32_t *code, sffn_stream_t
     if (!workspace || !code) return SFFN_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemcpyAsync(code, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
-    // clears the whole control block: the error word and the decode barrier
-    // words (left mid-count only by a call that recorded a timeout)
+    // clears the whole control block: the error word and the decode epoch,
+    // finish count and chunk flags (left mid-count only by a call that recorded
+    // a timeout)
     if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, kControlBytes, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return cuda_status(e);

@@ -9,6 +9,7 @@
 #include "sffn.h"
 
 #define SFFN_DEV __device__ __forceinline__
+#define SFFN_HOST_DEV __host__ __device__ __forceinline__
 
 namespace sffn {
 
@@ -93,6 +94,16 @@ SFFN_DEV uint64_t l2_evict_first_policy() {
 // accesses to shared memory.
 SFFN_DEV void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Per-thread asynchronous global -> shared copies (completion by
+// cp_async_wait_all); addresses aligned to the copy size.
+SFFN_DEV void cp_async_16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+SFFN_DEV void cp_async_4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+SFFN_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, multiple of 16).
 SFFN_DEV void bulk_prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -117,6 +128,11 @@ SFFN_DEV void bulk_load(void *dst_smem, const void *src, uint32_t bytes, uint64_
 // workspace or outputs, so completion of any kernel implies completion of all
 // earlier ones.
 SFFN_DEV void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Barrier over `count` threads (whole warps) of the CTA on hardware barrier id
+// (1..15; id 0 is __syncthreads).
+SFFN_DEV void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 // Allow the next kernel in the stream to begin launching its CTAs.
 SFFN_DEV void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -1,18 +1,16 @@
 // decode.cu -- activation-sparse gated-FFN decode GEMV kernels (sm_103a).
 //
 // One decode call runs, in stream order with programmatic dependent launch:
-//   gate     gate GEMV over all d_ff neurons + bias + act + score; for exact /
-//            threshold gating the per-neuron decision is taken here and each CTA
-//            compacts its chunk of neurons into an ascending index list
-//            (warp ballot + block prefix sum; no atomics, no inter-CTA waits).
-//   select   keep-ratio only: per-token radix select of the k-th largest score
-//            over the float bits (no sort), then ordered compaction.
-//   updown   persistent grid; every CTA scans the chunk counts, takes an equal
-//            share of the active neurons and streams only their W_up rows
-//            (dot with x) and W_downT rows (axpy into an fp32 partial held in
-//            registers, 8 output columns per thread, 128-bit loads).
-//   reduce   fixed-order sum of the per-CTA partials (deterministic), rounding to
-//            the output dtype; also writes the per-token ascending active lists.
+//   exact / threshold gating: one kernel (k_gate) streams the whole gate (and,
+//            for active neurons only, W_up and W_downT rows), decides, builds the
+//            ascending per-token lists, accumulates per-CTA partials and, with
+//            every CTA resident, finishes the output behind a bounded grid
+//            barrier (fixed-order sum: deterministic).  With more chunks than
+//            SMs, k_reduce finishes instead.
+//   keep-ratio: k_gate writes the scores; k_keep_ratio selects the k largest
+//            per token by radix select over the float bits (no sort); k_updown /
+//            k_down stream the selected W_up / W_downT rows into per-CTA
+//            partials; k_reduce sums them in a fixed order and writes the lists.
 //
 // The gated FFN and the skipping rules follow denseflux ("skipping most of a
 // dense FFN", sec. 1 and 5.1-5.3: only active rows of W_up / columns of W_down
@@ -168,15 +166,22 @@ __global__ void __launch_bounds__(256) k_down_norms(const void *wdT, const void 
 // gate kernel
 // ---------------------------------------------------------------------------
 //
-// One CTA per SM owns R consecutive neurons (a "chunk").  Lane 0 of warp 0
-// streams the chunk's gate rows (and, for the gate-and-up score, the up rows)
-// into a ring of shared-memory stages with 1-D bulk copies (TMA) completing on
-// mbarriers; eight consumer warps take one row each, form the dot products
-// from shared memory, apply bias / act / score and decide.  For the exact and
-// threshold rules a warp whose row is active for some token immediately reads
-// that neuron's W_up row and forms u_j and h_j = a_j * u_j, so the down kernel
-// needs nothing but (j, h_j).  Every mbarrier wait is time-bounded; on a timeout
-// the CTA records SFFN_ERR_TIMEOUT, drains its own copies and stops.
+// One CTA per SM owns R consecutive neurons (a "chunk").  Warp w of the CTA
+// streams rows w, w + 8, w + 16, ... of the chunk through its own ring of D
+// shared-memory stages (1-D bulk copies issued by its lane 0, one mbarrier per
+// stage) and forms the gate dot products (and, for the gate-and-up score, the
+// up dot products) against x held in registers, then bias, act, score and the
+// decision.  For the exact and threshold rules the item the warp puts into its
+// ring after an active row is that neuron's W_up row, so u_j and h_j = a_j u_j
+// are known when the gate stream ends; the neuron's W_downT row is prefetched
+// into L2 at the decision.  After the stream each CTA compacts its chunk into
+// ascending per-token lists, bulk-loads its active W_downT rows into the idle
+// ring and accumulates its fp32 partial of the output.  When all CTAs are
+// resident (grid <= #SMs) they then meet at a bounded grid barrier, sum
+// 32-column blocks of the partials in a fixed order and write their chunk's
+// lists; otherwise k_reduce does that.  Every wait is time-bounded; on a
+// timeout the CTA records SFFN_ERR_TIMEOUT, lets its own copies in flight land
+// and skips the rest of its work.
 
 struct GateArgs {
     const void *wg, *wu;
@@ -199,7 +204,7 @@ struct GateArgs {
     const void *sg, *su, *sd;  // int4: fp16 group scales [F, d/64] of gate, up, down
     // fused final reduction (all CTAs co-resident): grid barrier words in the
     // workspace, the output and the per-token index lists
-    unsigned *gbar;            // [2]: arrivals, phase (zero before first use; self-resetting)
+    unsigned *gbar;            // [2]: arrivals (never reset), arrivals before this call
     void *out;
     int out_f32;
     int32_t *active_idx, *n_active;
@@ -207,7 +212,74 @@ struct GateArgs {
 
 constexpr int kGateWarps = 8;           // each warp streams its own rows
 constexpr int kGateThreads = 32 * kGateWarps;
-constexpr int kMaxChunk = 256;  // R <= kMaxChunk <= blockDim: one scan pass compacts a chunk
+constexpr int kMaxChunk = 256;   // R <= kMaxChunk <= blockDim: one scan pass compacts a chunk
+constexpr int kMaxStages = 16;   // ring stages per warp
+constexpr int kMaxChunks = 256;  // C <= kMaxChunks <= blockDim: one scan pass over the chunk counts
+constexpr int kUpItem = 1 << 16; // ring item tag: the W_up row of the neuron in the low bits
+
+// Bytes of the gate kernel's mbarrier block (one per stage, one for the active
+// rows' copies after the stream), 128-byte aligned.
+SFFN_HOST_DEV uint32_t gate_bar_bytes(int D) { return ((uint32_t)((kGateWarps * D + 1) * 8) + 127u) & ~127u; }
+
+// Dot products of one stored row (and, with TWO, a second row) with the nb
+// tokens' activations: each lane takes units lane, lane + 32, ... (d_model <=
+// 4096), four independent accumulators per token and row.  x comes from
+// registers (xr, one token) or shared memory (xs).
+template <class W, int NB, bool TWO, bool XREG>
+SFFN_DEV void row_dots(const unsigned char *ra, const unsigned char *rb, uint32_t units, uint32_t row_bytes,
+                       const float *xr, const uint4 *xs, uint32_t xunits, float (&acca)[NB][4],
+                       float (&accb)[NB][4]) {
+    constexpr int UPL = 128 / W::E;         // units per lane at d_model <= 4096
+    constexpr int CU = W::E >= 32 ? 1 : 4;  // units loaded together (ILP)
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acca[b][c] = accb[b][c] = 0.f;
+#pragma unroll
+    for (int i0 = 0; i0 < UPL; i0 += CU) {
+        uint4 va[CU], vb[CU];
+        float sa[CU], sb[CU];
+#pragma unroll
+        for (int c = 0; c < CU; ++c) {
+            const uint32_t u = (i0 + c) * 32 + lane;
+            const bool in = u < units;
+            va[c] = in ? *reinterpret_cast<const uint4 *>(ra + u * 16) : make_uint4(0, 0, 0, 0);
+            sa[c] = W::Q && in ? W::scale_at(ra + row_bytes, u) : 1.f;
+            if (TWO) {
+                vb[c] = in ? *reinterpret_cast<const uint4 *>(rb + u * 16) : make_uint4(0, 0, 0, 0);
+                sb[c] = W::Q && in ? W::scale_at(rb + row_bytes, u) : 1.f;
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < CU; ++c) {
+            const uint32_t u = (i0 + c) * 32 + lane;
+            float fa[W::E], fb[W::E];
+            W::dequant(va[c], sa[c], fa);
+            if (TWO) W::dequant(vb[c], sb[c], fb);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                float xf[W::E];
+                if (XREG) {
+#pragma unroll
+                    for (int e = 0; e < W::E; ++e) xf[e] = xr[(i0 + c) * W::E + e];
+                } else if (u < units) {
+                    W::load_xu(xs + (size_t)b * xunits, u, xf);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < W::E; ++e) xf[e] = 0.f;
+                }
+#pragma unroll
+                for (int e = 0; e < W::E; ++e) {
+                    const int ai = CU == 1 ? (e & 3) : c;
+                    acca[b][ai] = fmaf(fa[e], xf[e], acca[b][ai]);
+                    if (TWO) accb[b][ai] = fmaf(fb[e], xf[e], accb[b][ai]);
+                }
+            }
+        }
+        if ((i0 + CU) * 32 >= (int)units) break;
+    }
+}
 
 template <class W, int NB, bool UP>
 __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
@@ -219,12 +291,15 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     const uint32_t rspace = row_bytes + sbytes;    // a row (codes, then scales) in shared memory
     const uint32_t stage_bytes = UP ? 2u * rspace : rspace;
     const uint32_t xunits = (uint32_t)(d * (int)sizeof(typename W::X) / 16);
-    const int D = a.stages;                        // stages (rows in flight) per warp
-    unsigned char *ring = smraw;                   // [warps][D] stages
-    unsigned char *xraw = smraw + (size_t)kGateWarps * D * stage_bytes;
-    const uint4 *xs = reinterpret_cast<const uint4 *>(xraw);   // x in its own dtype [NB][d]
-    uint64_t *full = reinterpret_cast<uint64_t *>(xraw + (size_t)NB * xunits * 16);  // [warps][D]
+    const int D = a.stages;                        // stages (items in flight) per warp
+    // dynamic shared memory: [warps][D] + 1 mbarriers | [warps][D] stages | x
+    uint64_t *full = reinterpret_cast<uint64_t *>(smraw);
     uint64_t *dbar = full + (size_t)kGateWarps * D;  // active-row copies after the stream
+    const uint32_t bar_bytes = gate_bar_bytes(D);
+    unsigned char *ring = smraw + bar_bytes;
+    unsigned char *xraw = ring + (size_t)kGateWarps * D * stage_bytes;
+    const uint4 *xs = reinterpret_cast<const uint4 *>(xraw);   // x in its own dtype [NB][d]
+    __shared__ int sitem[kGateWarps][kMaxStages];  // item in each stage: row, | kUpItem for its W_up row
     __shared__ uint8_t sflag[kMaxChunk];
     __shared__ float sh[kMaxChunk][NB];
     __shared__ float sbias[kMaxChunk], snorm[kMaxChunk];
@@ -236,15 +311,28 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     const int nrows = min(a.R, F - row0);
     // warp w handles rows w, w + 8, w + 16, ... of the chunk
     const int nmine = nrows > warp ? (nrows - warp + kGateWarps - 1) / kGateWarps : 0;
+    const bool up_items = a.decide && !UP;  // W_up rows of active neurons join the stream
     uint64_t *wfull = full + (size_t)warp * D;
     unsigned char *wring = ring + (size_t)warp * D * stage_bytes;
+    int *witem = sitem[warp];
     const char *gbase = static_cast<const char *>(a.wg) + (size_t)row0 * row_bytes;
-    const char *ubase = UP ? static_cast<const char *>(a.wu) + (size_t)row0 * row_bytes : nullptr;
+    const char *ubase = static_cast<const char *>(a.wu) + (size_t)row0 * row_bytes;
     const char *gsbase = W::Q ? static_cast<const char *>(a.sg) + (size_t)row0 * sbytes : nullptr;
-    const char *usbase = W::Q && UP ? static_cast<const char *>(a.su) + (size_t)row0 * sbytes : nullptr;
+    const char *usbase = W::Q ? static_cast<const char *>(a.su) + (size_t)row0 * sbytes : nullptr;
     uint64_t pol = 0;
-    // one stage: gate row codes [+ scales] [+ up row codes [+ scales]]
-    auto issue_row = [&](unsigned char *stage, size_t r, uint64_t *bar) {
+    // Put item `it` into stage s (lane 0): gate row codes [+ scales] [+ up row
+    // codes [+ scales]], or one W_up row for an up item.
+    auto issue = [&](int s, int it) {
+        unsigned char *stage = wring + (size_t)s * stage_bytes;
+        uint64_t *bar = &wfull[s];
+        const size_t r = (size_t)(it & (kUpItem - 1));
+        witem[s] = it;
+        if (it & kUpItem) {
+            mbar_arrive_expect_tx(bar, rspace);
+            bulk_load(stage, ubase + r * row_bytes, row_bytes, bar, pol);
+            if (W::Q) bulk_load(stage + row_bytes, usbase + r * sbytes, sbytes, bar, pol);
+            return;
+        }
         mbar_arrive_expect_tx(bar, stage_bytes);
         bulk_load(stage, gbase + r * row_bytes, row_bytes, bar, pol);
         if (W::Q) bulk_load(stage + row_bytes, gsbase + r * sbytes, sbytes, bar, pol);
@@ -253,16 +341,17 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
             if (W::Q) bulk_load(stage + rspace + row_bytes, usbase + r * sbytes, sbytes, bar, pol);
         }
     };
-    // Each warp keeps its own D row copies in flight (1-D bulk copies issued by
-    // its lane 0) and re-issues into a stage as soon as it has consumed it: no
-    // producer warp, so a slow warp never holds back another warp's stream.
-    // Weights are constant inputs: they stream before the dependency wait.
+    // Each warp keeps its own D items in flight and re-issues as soon as it has
+    // consumed one: no producer warp, so a slow warp never holds back another
+    // warp's stream.  Item i always sits in stage i % D.  Weights are constant
+    // inputs: they stream before the dependency wait.
+    int issued = min(D, nmine);  // items issued by this warp (warp-uniform)
+    int gnext = issued;          // gate rows issued: the warp's rows 0 .. gnext-1
     if (lane == 0) {
         for (int i = 0; i < D; ++i) mbar_init(&wfull[i], 1);
         mbar_fence_init();
         pol = l2_evict_first_policy();
-        for (int i = 0; i < D && i < nmine; ++i)
-            issue_row(wring + (size_t)i * stage_bytes, (size_t)(warp + i * kGateWarps), &wfull[i]);
+        for (int i = 0; i < issued; ++i) issue(i, warp + i * kGateWarps);
     }
     if (tid == 0) {
         s_abort = 0;
@@ -271,9 +360,11 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     }
     // x may be the previous layer's output: read it only after the dependency wait
     griddep_wait();
-    // the reduction may be scheduled now (its small CTAs fit beside this one);
-    // it waits for this grid's completion before reading the partials
+    // the reduction may be scheduled now (its small CTAs fit beside this one)
     griddep_launch_dependents();
+    // grid-barrier base: arrivals counted before this call (moves only after
+    // every CTA of this call has arrived)
+    const unsigned bar_base = a.gbar ? *reinterpret_cast<volatile unsigned *>(a.gbar + 1) : 0u;
     {
         constexpr int XE = 16 / (int)sizeof(typename W::X);
         const int per_row = d / XE, total = NB * per_row;
@@ -291,8 +382,7 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
         // This lane always handles units lane, lane + 32, ... of a row: for one
         // token its slice of x is unpacked into registers once and reused for
         // every row.  Units per lane <= UPL (d_model <= 4096).
-        constexpr int UPL = 128 / W::E;        // units per lane at d_model <= 4096
-        constexpr int CU = W::E >= 32 ? 1 : 4;  // units loaded together (ILP)
+        constexpr int UPL = 128 / W::E;
         constexpr bool XREG = NB == 1;
         float xr[XREG ? UPL * W::E : 1];
         if (XREG) {
@@ -307,10 +397,10 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
                     for (int e = 0; e < W::E; ++e) f[e] = 0.f;
                 }
 #pragma unroll
-                for (int e = 0; e < W::E; ++e) xr[(XREG ? i * W::E + e : 0)] = f[e];
+                for (int e = 0; e < W::E; ++e) xr[XREG ? i * W::E + e : 0] = f[e];
             }
         }
-        for (int k = 0; k < nmine; ++k) {
+        for (int k = 0; k < issued; ++k) {
             const int si = k % D;
             const bool ok = mbar_wait(&wfull[si], (uint32_t)(k / D) & 1u);
             if (!__all_sync(0xffffffffu, ok && !s_abort)) {
@@ -321,108 +411,92 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
                         s_abort = 1;
                         record_error(a.err, SFFN_ERR_TIMEOUT);
                     }
-                    for (int kk = k; kk < min(nmine, k + D); ++kk) mbar_wait(&wfull[kk % D], (uint32_t)(kk / D) & 1u);
+                    for (int kk = k; kk < issued; ++kk) mbar_wait(&wfull[kk % D], (uint32_t)(kk / D) & 1u);
                 }
                 __syncwarp();
                 break;
             }
-            {
-                const int r = warp + k * kGateWarps;
-                const unsigned char *st = wring + (size_t)si * stage_bytes;
-                // 4 independent accumulators per token and projection (ILP)
-                float accg[NB][4], accu[NB][4];
-#pragma unroll
-                for (int b = 0; b < NB; ++b)
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) accg[b][c] = accu[b][c] = 0.f;
-#pragma unroll
-                for (int i0 = 0; i0 < UPL; i0 += CU) {
-                    uint4 vg[CU], vu[CU];
-                    float scg[CU], scu[CU];
-#pragma unroll
-                    for (int c = 0; c < CU; ++c) {
-                        const uint32_t u = (i0 + c) * 32 + lane;
-                        const bool in = u < units;
-                        vg[c] = in ? *reinterpret_cast<const uint4 *>(st + u * 16) : make_uint4(0, 0, 0, 0);
-                        scg[c] = W::Q && in ? W::scale_at(st + row_bytes, u) : 1.f;
-                        if (UP) {
-                            vu[c] = in ? *reinterpret_cast<const uint4 *>(st + rspace + u * 16) : make_uint4(0, 0, 0, 0);
-                            scu[c] = W::Q && in ? W::scale_at(st + rspace + row_bytes, u) : 1.f;
-                        }
-                    }
-#pragma unroll
-                    for (int c = 0; c < CU; ++c) {
-                        const uint32_t u = (i0 + c) * 32 + lane;
-                        float fg[W::E], fu[W::E];
-                        W::dequant(vg[c], scg[c], fg);
-                        if (UP) W::dequant(vu[c], scu[c], fu);
-#pragma unroll
-                        for (int b = 0; b < NB; ++b) {
-                            float xf[W::E];
-                            if (XREG) {
-#pragma unroll
-                                for (int e = 0; e < W::E; ++e) xf[e] = xr[XREG ? (i0 + c) * W::E + e : 0];
-                            } else if (u < units) {
-                                W::load_xu(xs + (size_t)b * xunits, u, xf);
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < W::E; ++e) xf[e] = 0.f;
-                            }
-#pragma unroll
-                            for (int e = 0; e < W::E; ++e) {
-                                const int ai = CU == 1 ? (e & 3) : c;
-                                accg[b][ai] = fmaf(fg[e], xf[e], accg[b][ai]);
-                                if (UP) accu[b][ai] = fmaf(fu[e], xf[e], accu[b][ai]);
-                            }
-                        }
-                    }
-                    if ((i0 + CU) * 32 >= (int)units) break;
-                }
-                // stage consumed: refill it with this warp's row k + D
+            const int it = witem[si];
+            const int r = it & (kUpItem - 1);
+            const unsigned char *st = wring + (size_t)si * stage_bytes;
+            int next = -1;  // the item that goes into the ring after this one
+            if (it & kUpItem) {
+                // W_up row of an active neuron: u_j per token, h_j = a_j u_j
+                float acu[NB][4], unused[NB][4];
+                row_dots<W, NB, false, XREG>(st, nullptr, units, row_bytes, xr, xs, xunits, acu, unused);
                 __syncwarp();
-                if (lane == 0 && k + D < nmine) {
+                if (gnext < nmine) next = warp + (gnext++) * kGateWarps;
+                if (lane == 0 && next >= 0) {
                     fence_proxy_async_smem();
-                    issue_row(wring + (size_t)si * stage_bytes, (size_t)(warp + (k + D) * kGateWarps), &wfull[si]);
+                    issue(issued % D, next);
                 }
-                float g = 0.f, uu = 0.f;
+                float uu = 0.f;
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
-                    const float sg = warp_sum((accg[b][0] + accg[b][1]) + (accg[b][2] + accg[b][3]));
-                    const float su = UP ? warp_sum((accu[b][0] + accu[b][1]) + (accu[b][2] + accu[b][3])) : 0.f;
-                    if (lane == b) { g = sg; uu = su; }
+                    const float t = warp_sum((acu[b][0] + acu[b][1]) + (acu[b][2] + acu[b][3]));
+                    if (lane == b) uu = t;
                 }
-                const int j = row0 + r;
-                bool active = false;
-                float av = 0.f;
-                if (lane < a.nb) {
-                    g += sbias[r];
-                    av = act_fn(a.act, g);
-                    float sc = 0.f;
-                    if (a.score || (a.decide && a.mode != SFFN_MODE_EXACT)) {
-                        sc = (a.score_kind == SFFN_SCORE_GATE_UP ? fabsf(av * uu) : fabsf(av)) * snorm[r];
-                        if (a.score) a.score[(size_t)lane * F + j] = sc;
-                    }
-                    if (a.decide) {
-                        active = a.mode == SFFN_MODE_EXACT ? av != 0.f : sc >= a.tau;
-                    } else {
-                        if (a.aeff) a.aeff[(size_t)lane * F + j] = av;
-                        if (UP && a.uval) a.uval[(size_t)lane * F + j] = uu;
-                    }
-                }
-                if (!a.decide) continue;
-                const unsigned m = __ballot_sync(0xffffffffu, active) & 0xffu;
-                if (m != 0u && lane == 0) {
-                    bulk_prefetch_l2(static_cast<const char *>(a.wdT) + (size_t)j * row_bytes, row_bytes);
-                    if (!UP) bulk_prefetch_l2(static_cast<const char *>(a.wu) + (size_t)j * row_bytes, row_bytes);
-                    if (W::Q) {
-                        bulk_prefetch_l2(static_cast<const char *>(a.sd) + (size_t)j * sbytes, sbytes);
-                        if (!UP) bulk_prefetch_l2(static_cast<const char *>(a.su) + (size_t)j * sbytes, sbytes);
-                    }
-                }
-                // UP: h_j = a_j u_j now; otherwise the masked a_j, multiplied by u_j later
-                if (lane < NB) sh[r][lane] = active ? (UP ? av * uu : av) : 0.f;
-                if (lane == 0) sflag[r] = (uint8_t)m;
+                if (lane < a.nb) sh[r][lane] = ((sflag[r] >> lane) & 1u) ? sh[r][lane] * uu : 0.f;
+                if (next >= 0) ++issued;
+                continue;
             }
+            float accg[NB][4], accu[NB][4];
+            row_dots<W, NB, UP, XREG>(st, st + rspace, units, row_bytes, xr, xs, xunits, accg, accu);
+            __syncwarp();
+            if (!up_items) {
+                // stage consumed: refill it now with this warp's next gate row
+                if (gnext < nmine) next = warp + (gnext++) * kGateWarps;
+                if (lane == 0 && next >= 0) {
+                    fence_proxy_async_smem();
+                    issue(issued % D, next);
+                }
+                if (next >= 0) ++issued;
+            }
+            float g = 0.f, uu = 0.f;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float sg = warp_sum((accg[b][0] + accg[b][1]) + (accg[b][2] + accg[b][3]));
+                const float su = UP ? warp_sum((accu[b][0] + accu[b][1]) + (accu[b][2] + accu[b][3])) : 0.f;
+                if (lane == b) { g = sg; uu = su; }
+            }
+            const int j = row0 + r;
+            bool active = false;
+            float av = 0.f;
+            if (lane < a.nb) {
+                g += sbias[r];
+                av = act_fn(a.act, g);
+                float sc = 0.f;
+                if (a.score || (a.decide && a.mode != SFFN_MODE_EXACT)) {
+                    sc = (a.score_kind == SFFN_SCORE_GATE_UP ? fabsf(av * uu) : fabsf(av)) * snorm[r];
+                    if (a.score) a.score[(size_t)lane * F + j] = sc;
+                }
+                if (a.decide) {
+                    active = a.mode == SFFN_MODE_EXACT ? av != 0.f : sc >= a.tau;
+                } else {
+                    if (a.aeff) a.aeff[(size_t)lane * F + j] = av;
+                    if (UP && a.uval) a.uval[(size_t)lane * F + j] = uu;
+                }
+            }
+            if (!a.decide) continue;
+            const unsigned m = __ballot_sync(0xffffffffu, active) & 0xffu;
+            // UP: h_j = a_j u_j now; otherwise the masked a_j, times u_j when the
+            // W_up row (the next item) arrives
+            if (lane < NB) sh[r][lane] = active ? (UP ? av * uu : av) : 0.f;
+            if (lane == 0) sflag[r] = (uint8_t)m;
+            if (up_items) {
+                if (m != 0u) next = r | kUpItem;
+                else if (gnext < nmine) next = warp + (gnext++) * kGateWarps;
+                if (lane == 0 && next >= 0) {
+                    fence_proxy_async_smem();
+                    issue(issued % D, next);
+                }
+                if (next >= 0) ++issued;
+            }
+            if (m != 0u && lane == 0) {
+                bulk_prefetch_l2(static_cast<const char *>(a.wdT) + (size_t)j * row_bytes, row_bytes);
+                if (W::Q) bulk_prefetch_l2(static_cast<const char *>(a.sd) + (size_t)j * sbytes, sbytes);
+            }
+            __syncwarp();  // sh / sflag of this row before a later up item of the warp reads them
         }
     }
     __syncthreads();
@@ -452,36 +526,27 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     }
     __syncthreads();
 
-    // Active neurons of this chunk, in batches that fit the idle ring: their
-    // W_downT rows (and W_up rows unless u_j is known) come from L2 by bulk copy
-    // in one round trip; a warp per row forms u_j and h_j = a_j u_j; then every
-    // thread owns 16-byte column units and accumulates h_j * W_down[:, j] over
-    // the rows in ascending order (deterministic) into this CTA's partial.
+    // Active neurons of this chunk (h_j already known), in batches that fit the
+    // idle ring: their W_downT rows come from L2 (prefetched at the decision) by
+    // bulk copy in one round trip; then every thread owns 16-byte column units
+    // and accumulates h_j * W_down[:, j] over the rows in ascending order
+    // (deterministic) into this CTA's partial.
     const int ndown = failed ? 0 : s_ndown;
-    const int per_row_slots = UP ? 1 : 2;
-    const int cap = (int)((size_t)kGateWarps * D * stage_bytes / rspace) / per_row_slots;
+    const int cap = (int)((size_t)kGateWarps * D * stage_bytes / rspace);
     const char *wd = static_cast<const char *>(a.wdT);
-    const char *wu = static_cast<const char *>(a.wu);
     const char *sd = static_cast<const char *>(a.sd);
-    const char *suq = static_cast<const char *>(a.su);
-    const int nwarps = blockDim.x >> 5;
     for (int b0 = 0, batch = 0;; b0 += cap, ++batch) {
         const int bn = min(cap, ndown - b0);
         if (bn > 0) {
             if (tid == 0) {
                 fence_proxy_async_smem();  // earlier generic reads of the ring precede the copies
                 const uint64_t pol = l2_evict_first_policy();
-                mbar_arrive_expect_tx(dbar, (uint32_t)(bn * per_row_slots) * rspace);
+                mbar_arrive_expect_tx(dbar, (uint32_t)bn * rspace);
                 for (int i = 0; i < bn; ++i) {
                     const size_t j = (size_t)(row0 + sdown[b0 + i]);
                     unsigned char *dslot = ring + (size_t)i * rspace;
                     bulk_load(dslot, wd + j * row_bytes, row_bytes, dbar, pol);
                     if (W::Q) bulk_load(dslot + row_bytes, sd + j * sbytes, sbytes, dbar, pol);
-                    if (!UP) {
-                        unsigned char *uslot = ring + (size_t)(cap + i) * rspace;
-                        bulk_load(uslot, wu + j * row_bytes, row_bytes, dbar, pol);
-                        if (W::Q) bulk_load(uslot + row_bytes, suq + j * sbytes, sbytes, dbar, pol);
-                    }
                 }
             }
             const bool ok = mbar_wait(dbar, (uint32_t)batch & 1u);
@@ -489,59 +554,6 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
                 if (tid == 0) record_error(a.err, SFFN_ERR_TIMEOUT);
                 failed = true;
                 break;
-            }
-            if (!UP) {
-                constexpr int UPL = 128 / W::E;        // units per lane (d_model <= 4096)
-                constexpr int CU = W::E >= 32 ? 1 : 4;
-                for (int i = warp; i < bn; i += nwarps) {
-                    const unsigned char *ur = ring + (size_t)(cap + i) * rspace;
-                    float su[NB][4];
-#pragma unroll
-                    for (int b = 0; b < NB; ++b)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) su[b][c] = 0.f;
-#pragma unroll
-                    for (int i0 = 0; i0 < UPL; i0 += CU) {
-                        uint4 v[CU];
-                        float sc[CU];
-#pragma unroll
-                        for (int c = 0; c < CU; ++c) {
-                            const uint32_t u = (i0 + c) * 32 + lane;
-                            const bool in = u < units;
-                            v[c] = in ? *reinterpret_cast<const uint4 *>(ur + u * 16) : make_uint4(0, 0, 0, 0);
-                            sc[c] = W::Q && in ? W::scale_at(ur + row_bytes, u) : 1.f;
-                        }
-#pragma unroll
-                        for (int c = 0; c < CU; ++c) {
-                            const uint32_t u = (i0 + c) * 32 + lane;
-                            float f[W::E];
-                            W::dequant(v[c], sc[c], f);
-#pragma unroll
-                            for (int b = 0; b < NB; ++b) {
-                                float xf[W::E];
-                                if (u < units) {
-                                    W::load_xu(xs + (size_t)b * xunits, u, xf);
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < W::E; ++e) xf[e] = 0.f;
-                                }
-#pragma unroll
-                                for (int e = 0; e < W::E; ++e) {
-                                    const int ai = CU == 1 ? (e & 3) : c;
-                                    su[b][ai] = fmaf(f[e], xf[e], su[b][ai]);
-                                }
-                            }
-                        }
-                        if ((i0 + CU) * 32 >= (int)units) break;
-                    }
-                    const int r = sdown[b0 + i];
-#pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        const float t = warp_sum((su[b][0] + su[b][1]) + (su[b][2] + su[b][3]));
-                        if (lane == b) sh[r][b] *= t;  // h = a_j * u_j
-                    }
-                }
-                __syncthreads();
             }
         }
         for (uint32_t u = tid; u < units; u += blockDim.x) {
@@ -578,23 +590,19 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
 
     // ---- grid barrier: every CTA's partial and chunk counts are written ----
     // One CTA per SM and grid <= #SMs, so all CTAs are resident; the wait is
-    // bounded all the same.  gbar[0] counts arrivals and is back at 0 when the
-    // barrier opens; gbar[1] is the phase the last arrival advances.
+    // bounded all the same.  gbar[0] counts arrivals and is never reset; this
+    // call's barrier opens once it has grown by gridDim.x past the base
+    // (unsigned differences, so wrap-around is harmless).
     __shared__ int s_bar_ok;
     __threadfence();
     __syncthreads();
     if (tid == 0) {
-        volatile unsigned *vphase = a.gbar + 1;
-        const unsigned phase = *vphase;
-        __threadfence();  // the phase is read before this CTA's arrival counts
+        atomicAdd(a.gbar, 1u);
+        const volatile unsigned *arrivals = a.gbar;
         int ok = 1;
-        if (atomicAdd(a.gbar, 1u) == gridDim.x - 1) {
-            atomicExch(a.gbar, 0u);
-            __threadfence();
-            atomicExch(a.gbar + 1, phase + 1u);
-        } else {
+        if (*arrivals - bar_base < gridDim.x) {
             const uint64_t t0 = globaltimer_ns();
-            while (*vphase == phase)
+            while (*arrivals - bar_base < gridDim.x)
                 if (globaltimer_ns() - t0 > kWaitLimitNs) {
                     ok = 0;
                     record_error(a.err, SFFN_ERR_TIMEOUT);
@@ -605,51 +613,67 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
         s_bar_ok = ok;
     }
     __syncthreads();
+    // every CTA read the base before it arrived: the next call's base can be
+    // published now (the next call reads it after this grid has completed)
+    if (blockIdx.x == 0 && tid == 0) *reinterpret_cast<volatile unsigned *>(a.gbar + 1) = bar_base + gridDim.x;
     if (!s_bar_ok || failed) return;
 
-    // ---- output columns: blocks of 32, sums over the C partials in a fixed order
-    {
-        float *red = &sh[0][0];  // [8][32] (sh holds >= 256 floats and is free now)
-        const int lane32 = tid & 31, grp = tid >> 5;   // 8 groups of 32 threads
+    if (warp < 4) {
+        // ---- output: 32-column blocks, partials summed in a fixed order (warp
+        // g adds partials g, g + 4, ...; then the 4 warps in order)
+        float *red = &sh[0][0];  // [4][32] (sh holds >= 256 floats and is free now)
         const size_t total = (size_t)a.nb * d;
         const int C = gridDim.x;
         for (size_t cb = (size_t)blockIdx.x * 32; cb < total; cb += (size_t)C * 32) {
-            const size_t col = cb + lane32;
+            const size_t col = cb + lane;
             float sum = 0.f;
             if (col < total) {
-                float v[32];
+                // all of this thread's loads in flight at once (C <= 160 in one go)
+                float v[40];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int pp = grp + 8 * i;
+                for (int i = 0; i < 40; ++i) {
+                    const int pp = warp + 4 * i;
                     v[i] = pp < C ? __ldcg(a.part + (size_t)pp * total + col) : 0.f;
                 }
 #pragma unroll
-                for (int i = 0; i < 32; ++i) sum += v[i];
-                for (int pp = grp + 256; pp < C; pp += 8) sum += __ldcg(a.part + (size_t)pp * total + col);
+                for (int i = 0; i < 40; ++i) sum += v[i];
+                for (int pp = warp + 160; pp < C; pp += 4) sum += __ldcg(a.part + (size_t)pp * total + col);
             }
-            red[grp * 32 + lane32] = sum;
-            __syncthreads();
-            if (grp == 0 && col < total) {
-                float t = red[lane32];
-#pragma unroll
-                for (int g2 = 1; g2 < 8; ++g2) t += red[g2 * 32 + lane32];
+            red[warp * 32 + lane] = sum;
+            named_barrier_sync(1, 128);
+            if (warp == 0 && col < total) {
+                const float t = ((red[lane] + red[32 + lane]) + red[64 + lane]) + red[96 + lane];
                 if (a.out_f32) static_cast<float *>(a.out)[col] = t;
                 else static_cast<uint16_t *>(a.out)[col] = f32_to_bf16_bits(t);
             }
-            __syncthreads();
+            named_barrier_sync(1, 128);
         }
-    }
-    // ---- this chunk's ascending index lists at their global positions
-    for (int b = 0; b < a.nb; ++b) {
-        const int *cnt = a.cnt + (size_t)b * a.C;
-        int sacc = 0;
-        for (int c = tid; c < (int)blockIdx.x; c += blockDim.x) sacc += __ldcg(cnt + c);
-        int off;
-        block_excl_scan(sacc, scan_tmp, &off);
-        const int mine = __ldcg(cnt + blockIdx.x);
-        for (int i = tid; i < mine; i += blockDim.x)
-            a.active_idx[(size_t)b * F + off + i] = __ldcg(a.lidx + (size_t)b * F + row0 + i);
-        if (blockIdx.x == gridDim.x - 1 && tid == 0) a.n_active[b] = off + mine;
+    } else {
+        // ---- meanwhile: this chunk's ascending index lists at their global
+        // positions (warp 4 + k takes tokens k, k + 4, ...)
+        for (int b = warp - 4; b < a.nb; b += 4) {
+            const int *cnt = a.cnt + (size_t)b * a.C;
+            // counts of the earlier chunks (C <= kMaxChunks = 256: 8 per lane, in
+            // flight together) and this chunk's entries (R <= 256: 8 per lane)
+            int cv[8], ev[8];
+            const int mine = __ldcg(cnt + blockIdx.x);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int c = lane + 32 * i, e = lane + 32 * i;
+                cv[i] = c < (int)blockIdx.x ? __ldcg(cnt + c) : 0;
+                ev[i] = e < a.R && row0 + e < F ? __ldcg(a.lidx + (size_t)b * F + row0 + e) : 0;
+            }
+            int sacc = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sacc += cv[i];
+            const int off = __reduce_add_sync(0xffffffffu, sacc);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                if (e < mine) a.active_idx[(size_t)b * F + off + e] = ev[i];
+            }
+            if (blockIdx.x == gridDim.x - 1 && lane == 0) a.n_active[b] = off + mine;
+        }
     }
 }
 
@@ -1219,7 +1243,7 @@ DecodePlan make_decode_plan(int B, int d, int F) {
     p.d = d;
     p.F = F;
     const int sms = device_sm_count();
-    int C = sms;                         // one gate CTA per SM
+    int C = sms < kMaxChunks ? sms : kMaxChunks;  // one gate CTA per SM
     if (C > F) C = F;
     int R = (F + C - 1) / C;
     if (R > kMaxChunk) R = kMaxChunk;
@@ -1229,10 +1253,8 @@ DecodePlan make_decode_plan(int B, int d, int F) {
     p.nlists = B + (B > 1 ? 1 : 0);
     p.list_u = B > 1 ? B : 0;
     size_t o = 0;
-    // control block: error word, then the gate kernel's grid-barrier words
-    p.off_err = o;
-    p.off_bar = o + sizeof(int32_t);
-    o = align_up(o + sizeof(int32_t) + 2 * sizeof(unsigned));
+    p.off_err = o;  // the control block: error word, grid-barrier counters
+    o = align_up(o + kControlBytes);
     p.off_cnt = o; o = align_up(o + sizeof(int) * (size_t)p.nlists * p.C);
     p.off_lidx = o; o = align_up(o + sizeof(int) * (size_t)p.nlists * F);
     p.off_lh = o; o = align_up(o + sizeof(float) * (size_t)B * F);
@@ -1247,7 +1269,7 @@ DecodePlan make_decode_plan(int B, int d, int F) {
 
 // Dynamic shared memory of the gate kernel with D rows in flight per warp.
 static size_t gate_smem(size_t x_bytes, uint32_t stage_bytes, int D) {
-    return (size_t)kGateWarps * D * stage_bytes + x_bytes + sizeof(uint64_t) * ((size_t)kGateWarps * D + 1);
+    return gate_bar_bytes(D) + (size_t)kGateWarps * D * stage_bytes + x_bytes;
 }
 
 template <class W, int NB, bool UP>
@@ -1317,7 +1339,7 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     // exact / threshold with every gate CTA resident: the gate kernel finishes
     // the call itself (grid barrier + distributed reduction + index lists)
     const bool fused = !scores_only && !keep && p.C <= device_sm_count();
-    ga.gbar = fused ? reinterpret_cast<unsigned *>(ws + p.off_bar) : nullptr;
+    ga.gbar = fused ? reinterpret_cast<unsigned *>(ws + p.off_err + kCtlBar) : nullptr;
     ga.out = c.out;
     ga.out_f32 = w->wdtype == SFFN_F32;
     ga.active_idx = c.active_idx;

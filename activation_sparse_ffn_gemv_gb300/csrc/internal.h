@@ -13,10 +13,14 @@ namespace sffn {
 
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
-// Every workspace starts with a control block: the device error word (int32 at
-// byte 0) and the decode gate kernel's grid-barrier words (two uint32 at byte 4).
-// Only decode writes the barrier words, and each decode call leaves them zero.
-constexpr size_t kControlBytes = 12;
+// Every workspace starts with a control block of kControlBytes:
+//   byte 0  int32  device error word (any entry point)
+//   byte 4  uint32 decode grid barrier: arrivals, never reset (wraps)
+//   byte 8  uint32 decode grid barrier: arrivals before the current call
+// Only decode writes bytes 4 .. 11; a zero-filled control block is a valid
+// start, and every call leaves it valid for the next one.
+constexpr size_t kControlBytes = 16;
+constexpr size_t kCtlBar = 4;
 
 // SM count of the current device (cached per device).
 int device_sm_count();
@@ -56,7 +60,7 @@ struct DecodePlan {
     int nlists;   // nb per-token lists (+1 union list when nb > 1)
     int list_u;   // index of the list the up/down kernel walks
     // workspace offsets (bytes)
-    size_t off_err, off_bar, off_cnt, off_lidx, off_lh, off_aeff, off_uval, off_score, off_mask, off_part, total;
+    size_t off_err, off_cnt, off_lidx, off_lh, off_aeff, off_uval, off_score, off_mask, off_part, total;
 };
 
 DecodePlan make_decode_plan(int B, int d, int F);

@@ -47,8 +47,9 @@ extern "C" sffn_status sffn_decode_noalloc(const void *x, int B, const sffn_ffn_
     void *ws = scratch_address(dev);
     if (!ws) return SFFN_ERR_CUDA;
     // The array keeps whatever the previous call left; the decode kernels write
-    // every scratch word before reading it, except the control block (error word
-    // and grid-barrier words), which is cleared here so that each call starts clean.
+    // every scratch word before reading it, except the control block (error word,
+    // epoch, finish count, chunk flags), which is cleared here so that each call
+    // starts clean.
     if (cudaMemsetAsync(ws, 0, sffn::kControlBytes, (cudaStream_t)stream) != cudaSuccess) return SFFN_ERR_CUDA;
     return sffn_decode(x, B, w, mode, score, param, out, active_idx, n_active, ws,
                        (size_t)SFFN_NOALLOC_SCRATCH_BYTES, stream);

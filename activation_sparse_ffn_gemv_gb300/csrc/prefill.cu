@@ -398,7 +398,7 @@ PrefillPlan make_prefill_plan(int L, int d, int F) {
     p.d = d;
     p.F = F;
     size_t o = 0;
-    p.off_err = o; o = align_up(o + sizeof(int32_t));
+    p.off_err = o; o = align_up(o + kControlBytes);  // the control block
     p.off_ysel = o; o = align_up(o + sizeof(uint16_t) * (size_t)L * d);
     p.off_h = o; o = align_up(o + sizeof(uint16_t) * (size_t)L * F);
     p.total = o;

@@ -291,7 +291,7 @@ SelectPlan make_select_plan(int L, int d) {
     p.L = L;
     p.d = d;
     size_t o = 0;
-    p.off_err = o; o = align_up(o + sizeof(int32_t));
+    p.off_err = o; o = align_up(o + kControlBytes);  // the control block
     p.off_norms = o; o = align_up(o + sizeof(float) * (size_t)L);
     p.off_flag = o; o = align_up(o + (size_t)L);
     p.total = o;

@@ -30,13 +30,13 @@
  *    The caller owns all memory and the stream; the library never allocates
  *    or frees on these calls: scratch memory comes from the caller's
  *    `workspace` (size from sffn_workspace_size, 256-byte aligned).
- *  - The first 256 bytes of every workspace are a control block: the device
- *    error word (below) and two words with which sffn_decode's CTAs meet at a
- *    grid barrier.  Zero-fill a workspace once before its first use (one
+ *  - The first 16 bytes of every workspace are a control block: the device
+ *    error word (below) and two counters with which sffn_decode's CTAs meet at
+ *    a grid barrier.  Zero-fill a workspace once before its first use (one
  *    cudaMemset at allocation); every call leaves the control block valid for
  *    the next one, whichever entry point it is, and sffn_read_device_error
- *    clears it.  A workspace serves one call at a time (calls on one stream, or
- *    ordered between streams).
+ *    clears it.  A workspace serves one call at a time (calls on one stream,
+ *    or ordered between streams).
  *  - Calls are asynchronous and stream-ordered on `stream` (NULL = the legacy
  *    default stream); nothing is read back to the host, so a sequence of calls
  *    can be captured in a CUDA graph.  Counts (n_active, n_sel) stay on the

@@ -182,3 +182,25 @@ def test_int4_keep_ratio_unsupported(sffn):
     with pytest.raises(sffn.SffnError) as e:
         sffn.decode(x, w, sffn.MODE_KEEP_RATIO, sffn.SCORE_GATE, 0.5)
     assert e.value.status == sffn.ERR_UNSUPPORTED
+
+
+# More neurons than (#SMs x 256): the gate kernel's chunks cannot all be resident
+# at once, so the lists and output slices are formed by a separate kernel.
+BIG_F = [
+    # (cfg, d, F, wdtype, mode, score, B)
+    (2, 64, 40000, "bf16", "exact", "gate", 1),
+    (2, 72, 39001, "bf16", "exact", "gate", 3),
+    (1, 32, 40960, "f32", "threshold", "gate_up", 2),
+    (4, 512, 40000, "int4_g64", "threshold", "gate", 1),
+]
+
+
+@pytest.mark.parametrize("case", BIG_F, ids=lambda c: "-".join(map(str, c)))
+def test_more_chunks_than_sms(sffn, case):
+    cfg, d, F, wd, mode, score, B = case
+    layer = W.make_ffn_layer(cfg, seed=41, d_model=d, d_ff=F, wdtype=wd,
+                             act="silu" if wd == "int4_g64" else "relu")
+    x = W.make_tokens(cfg, B, seed=9, d_model=d, xdtype="f32" if wd == "f32" else "bf16")
+    tau = _tau_at(layer, x, 0.85, score) if mode == "threshold" else 0.0
+    r = run_and_check_decode(sffn, layer, x, mode, score, tau, nthreads=16)
+    assert (r["n_active"] > 0).all()
