@@ -240,7 +240,12 @@ def run_ours(args):
     value = ms_max * 1e3 / total_tokens
     hbm, bf16_peak, bf16_sus, peak_src = peaks()
     achieved = bytes_tok / (us_tok * 1e-6) / 1e9
-    kernels_per_call = 2  # fused gate/down kernel + reduction
+    # one fused kernel per call when every gate chunk's CTA is resident (the
+    # decode plan: C = ceil(F / R) chunks, R = ceil(F / min(#SMs, 256)) <= 256),
+    # else the gate kernel and the reduction
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    R = min(256, -(-F // min(sms, 256, F)))
+    kernels_per_call = 1 if -(-F // R) <= sms else 2
     res = None
     if rank == 0:
         res = {
@@ -255,7 +260,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "active_fraction": round(a, 5),
             "gbps": round(achieved, 1),
-            "roofline": {"bound": "hbm", "kernel": "sffn_decode call (gate+sparse up/down kernel, reduction)",
+            "roofline": {"bound": "hbm", "kernel": "sffn_decode call (one kernel: gate stream, active up/down rows, grid-barrier reduction)",
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peak_src,
                          "bytes_per_launch": round(bytes_tok), "traffic": traffic_for("decode_exact_llama")},
@@ -376,7 +381,10 @@ def bench_decode_sweeps(args, dev, T=256):
     del layers, ws, sc_ws
     pts = [(sffn.MODE_THRESHOLD, sffn.SCORE_GATE, [taus[l][i] if c["sweep_a"][i] < 1.0 else 0.0 for l in range(nl)])
            for i in range(len(c["sweep_a"]))]
-    pts.append((sffn.MODE_THRESHOLD, sffn.SCORE_GATE, [0.0] * nl))  # dense: tau = 0 keeps all
+    # dense reference: every neuron (tau = 0 on the gate-and-up score keeps all), the
+    # gate and up rows streamed together and every W_downT row read: the dense FFN
+    # bytes (3 matrices) through the same kernels, without the skip
+    pts.append((sffn.MODE_THRESHOLD, sffn.SCORE_GATE_UP, [0.0] * nl))
     cfg, _, _, _, res = run_points(4, nl, pts)
     dense_us = res[-1][0]
     r = rowb(cfg)
@@ -387,15 +395,25 @@ def bench_decode_sweeps(args, dev, T=256):
         sweep.append({"a_target": a_t, "a": round(a, 4), "us_per_token": round(us, 3),
                       "gbps": round(b / (us * 1e-6) / 1e9, 1), "frac_hbm": round(b / (us * 1e-6) / 1e9 / hbm, 4),
                       "speedup_vs_dense": round(dense_us / us, 3)})
+    # breakeven: the active fraction where the sparse call takes as long as the
+    # dense one (linear between the swept points; "<" / ">" outside the sweep)
     be = None
     for p0, p1 in zip(sweep, sweep[1:]):
-        if p0["us_per_token"] <= dense_us <= p1["us_per_token"]:
-            be = p0["a"] + (dense_us - p0["us_per_token"]) * (p1["a"] - p0["a"]) / (
-                p1["us_per_token"] - p0["us_per_token"])
+        if p0["us_per_token"] <= dense_us <= p1["us_per_token"] and p1["us_per_token"] > p0["us_per_token"]:
+            be = round(p0["a"] + (dense_us - p0["us_per_token"]) * (p1["a"] - p0["a"]) / (
+                p1["us_per_token"] - p0["us_per_token"]), 3)
+            break
+    if be is None and sweep:
+        if sweep[0]["us_per_token"] > dense_us:
+            be = f"< {sweep[0]['a']}"
+        elif sweep[-1]["us_per_token"] < dense_us:
+            be = f"> {sweep[-1]['a']}"
     out["int4_threshold_sweep"] = {"workload": "qwen2.5-3b-swiglu-int4g64: d_model 2048, d_ff 11008, 36 layers, "
                                                "threshold on |SiLU(g)|*||W_down[:,j]||, B=1",
-                                   "dense_us_per_token": round(dense_us, 3), "points": sweep,
-                                   "breakeven_active_fraction": None if be is None else round(be, 3)}
+                                   "dense_us_per_token": round(dense_us, 3),
+                                   "dense": "every neuron: threshold 0 on the gate-and-up score (gate and up rows "
+                                            "streamed together), every W_downT row",
+                                   "points": sweep, "breakeven_active_fraction": be}
     torch.cuda.empty_cache()
 
     # keep-ratio tiers (gate-and-up score)
