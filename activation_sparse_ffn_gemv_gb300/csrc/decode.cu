@@ -70,13 +70,18 @@ struct WINT4 {
     }
     // nibble n (two's complement) -> n ^ 8 is the code + 8 as an unsigned value;
     // OR-ing it into the mantissa of 2^23 gives 2^23 + code + 8 exactly
-    static SFFN_DEV void dequant(const uint4 &v, float s, float *f) {
+    static SFFN_DEV void codes(const uint4 &v, float *f) {
         const uint32_t w[4] = {v.x ^ 0x88888888u, v.y ^ 0x88888888u, v.z ^ 0x88888888u, v.w ^ 0x88888888u};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                f[8 * q + k] = (__uint_as_float(0x4B000000u | ((w[q] >> (4 * k)) & 0xFu)) - 8388616.0f) * s;
+                f[8 * q + k] = __uint_as_float(0x4B000000u | ((w[q] >> (4 * k)) & 0xFu)) - 8388616.0f;
+    }
+    static SFFN_DEV void dequant(const uint4 &v, float s, float *f) {
+        codes(v, f);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) f[e] *= s;
     }
     static SFFN_DEV void load_xu(const uint4 *xrow, uint32_t u, float *f) {
 #pragma unroll
@@ -254,6 +259,36 @@ SFFN_DEV void row_dots(const unsigned char *ra, const unsigned char *rb, uint32_
 #pragma unroll
         for (int c = 0; c < CU; ++c) {
             const uint32_t u = (i0 + c) * 32 + lane;
+            if constexpr (W::Q) {
+                // group-scaled codes: the unit's 32 exact small-integer codes are
+                // dotted with x, then multiplied by the group scale once
+                float fa[W::E], fb[W::E];
+                W::codes(va[c], fa);
+                if (TWO) W::codes(vb[c], fb);
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    float xf[W::E];
+                    if (XREG) {
+#pragma unroll
+                        for (int e = 0; e < W::E; ++e) xf[e] = xr[(i0 + c) * W::E + e];
+                    } else if (u < units) {
+                        W::load_xu(xs + (size_t)b * xunits, u, xf);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < W::E; ++e) xf[e] = 0.f;
+                    }
+                    float pa[4] = {0.f, 0.f, 0.f, 0.f}, pb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int e = 0; e < W::E; ++e) {
+                        pa[e & 3] = fmaf(fa[e], xf[e], pa[e & 3]);
+                        if (TWO) pb[e & 3] = fmaf(fb[e], xf[e], pb[e & 3]);
+                    }
+                    const int ai = (i0 + c) & 3;
+                    acca[b][ai] = fmaf(sa[c], (pa[0] + pa[1]) + (pa[2] + pa[3]), acca[b][ai]);
+                    if (TWO) accb[b][ai] = fmaf(sb[c], (pb[0] + pb[1]) + (pb[2] + pb[3]), accb[b][ai]);
+                }
+                continue;
+            }
             float fa[W::E], fb[W::E];
             W::dequant(va[c], sa[c], fa);
             if (TWO) W::dequant(vb[c], sb[c], fb);

@@ -100,33 +100,77 @@ struct SelectArgs {
     int L;
     float mass_thresh;
     int recent_n, min_keep;
-    uint8_t *flag;         // [L] workspace
+    uint8_t *flag;         // [L] workspace (used when the keys are not staged)
+    int staged;            // 1: keys and flags live in dynamic shared memory (L <= kStageKeys)
     int32_t *sel_idx, *n_sel;
 };
 
+// Up to this many importances (and their flags) are staged in shared memory,
+// so that every pass of the selection reads on-chip memory.
+constexpr int kStageKeys = 32768;
+
 // One radix pass over the candidate keys (kv & pmask) == prefix, flag-filtered.
 // Histogram counts and (optionally) fixed-point masses per bin of the digit at `sh`.
+// Fixed-point mass of an importance v >= 0: v * 2^(40 - ex) rounded to the
+// nearest integer (ties to even), from the float's bits with integer shifts
+// only (no FP64 on the path).  With max importance < 2^ex every value is below
+// 2^40 units.
+SFFN_DEV unsigned long long fixed_mass(float v, int ex) {
+    const uint32_t u = __float_as_uint(v);
+    const int e = (int)((u >> 23) & 0xFFu);
+    const unsigned long long m = (u & 0x7FFFFFu) | (e ? 0x800000u : 0u);  // v = m * 2^(max(e,1) - 150)
+    if (m == 0ull || e == 0xFF) return 0ull;
+    const int sh = (e ? e : 1) - 150 + 40 - ex;
+    if (sh >= 0) return m << sh;
+    const int r = -sh;
+    if (r > 24) return 0ull;  // m < 2^24 <= half a unit
+    const unsigned long long q = m >> r, rem = m & ((1ull << r) - 1ull), half = 1ull << (r - 1);
+    return q + ((rem > half || (rem == half && (q & 1ull))) ? 1ull : 0ull);
+}
+
 template <bool MASS>
-SFFN_DEV void radix_hist(const SelectArgs &a, const uint8_t *exclude, uint32_t prefix, uint32_t pmask, int sh,
-                         int nbins, double scale, unsigned *hcnt, unsigned long long *hmass) {
+SFFN_DEV void radix_hist(const float *sv, int L, const uint8_t *exclude, uint32_t prefix, uint32_t pmask, int sh,
+                         int nbins, int ex, unsigned *hcnt, unsigned long long *hmass) {
     for (int i = threadIdx.x; i < nbins; i += blockDim.x) {
         hcnt[i] = 0;
         if (MASS) hmass[i] = 0;
     }
     __syncthreads();
-    for (int t = threadIdx.x; t < a.L; t += blockDim.x) {
-        if (exclude && exclude[t]) continue;
-        const float v = a.s[t];
-        const uint32_t kv = __float_as_uint(v);
-        if ((kv & pmask) != prefix) continue;
-        const int bin = (kv >> sh) & (nbins - 1);
-        atomicAdd(&hcnt[bin], 1u);
-        if (MASS) atomicAdd(&hmass[bin], (unsigned long long)__double2ull_rn((double)v * scale));
+    // Importances crowd into few bins, so lanes holding the same bin first add up
+    // their count and mass inside the warp (match + reduce; a fixed-point mass is
+    // below 2^40 and is summed as two 20-bit halves, exactly), then one lane per
+    // bin updates shared memory.  The loop is warp-uniform.
+    constexpr int U = 8;  // keys in flight per thread
+    const int lane = threadIdx.x & 31;
+    for (int t0 = threadIdx.x - lane; t0 < L; t0 += U * blockDim.x) {
+        float v[U];
+        bool ok[U];
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const int t = t0 + lane + k * blockDim.x;
+            ok[k] = t < L && !(exclude && exclude[t]);
+            v[k] = ok[k] ? sv[t] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+            const uint32_t kv = __float_as_uint(v[k]);
+            const int bin = ok[k] && (kv & pmask) == prefix ? (int)((kv >> sh) & (uint32_t)(nbins - 1)) : nbins;
+            const unsigned peers = __match_any_sync(0xffffffffu, bin);
+            const bool leader = lane == __ffs(peers) - 1;
+            if (MASS) {
+                const unsigned long long m = bin < nbins ? fixed_mass(v[k], ex) : 0ull;
+                const unsigned lo = __reduce_add_sync(peers, (unsigned)(m & 0xFFFFFull));
+                const unsigned hi = __reduce_add_sync(peers, (unsigned)(m >> 20));
+                if (leader && bin < nbins) atomicAdd(&hmass[bin], ((unsigned long long)hi << 20) + lo);
+            }
+            if (leader && bin < nbins) atomicAdd(&hcnt[bin], (unsigned)__popc(peers));
+        }
     }
     __syncthreads();
 }
 
 __global__ void __launch_bounds__(kSelectThreads) k_mass_select(SelectArgs a) {
+    extern __shared__ __align__(16) unsigned char sstage[];  // staged: [L] keys, then [L] flags
     __shared__ unsigned hcnt[2048];
     __shared__ unsigned long long hmass[2048];
     __shared__ unsigned long long scr64[33];
@@ -139,11 +183,34 @@ __global__ void __launch_bounds__(kSelectThreads) k_mass_select(SelectArgs a) {
     griddep_launch_dependents();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int L = a.L;
+    // keys and flags: shared memory when they fit (one coalesced pass, eight
+    // loads in flight per thread), else the workspace
+    const float *sv = a.s;
+    uint8_t *fl = a.flag;
+    if (a.staged) {
+        float *ss = reinterpret_cast<float *>(sstage);
+        for (int t0 = tid; t0 < L; t0 += 8 * blockDim.x) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int t = t0 + k * blockDim.x;
+                v[k] = t < L ? a.s[t] : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int t = t0 + k * blockDim.x;
+                if (t < L) ss[t] = v[k];
+            }
+        }
+        sv = ss;
+        fl = sstage + (size_t)L * sizeof(float);
+        __syncthreads();
+    }
 
     // maximum importance -> fixed-point scale: every value < 2^40 units, so a
     // sum of up to 2^20 values stays below 2^60
     float mx = 0.f;
-    for (int t = tid; t < L; t += blockDim.x) mx = fmaxf(mx, a.s[t]);
+    for (int t = tid; t < L; t += blockDim.x) mx = fmaxf(mx, sv[t]);
     mx = warp_max(mx);
     if (lane == 0) s_red[warp] = mx;
     __syncthreads();
@@ -157,15 +224,14 @@ __global__ void __launch_bounds__(kSelectThreads) k_mass_select(SelectArgs a) {
     __syncthreads();
     int ex = 0;
     if (mx > 0.f) frexpf(mx, &ex);                     // mx < 2^ex
-    const double scale = ldexp(1.0, 40 - ex);
     unsigned long long part = 0;
-    for (int t = tid; t < L; t += blockDim.x) part += __double2ull_rn((double)a.s[t] * scale);
+    for (int t = tid; t < L; t += blockDim.x) part += fixed_mass(sv[t], ex);
     unsigned long long total;
     block_excl_scan_u64(part, scr64, &total);
 
     // ---- mass prefix: flag[t] = 1 for the selected prefix
     const bool all = a.mass_thresh >= 1.f || total == 0ull;
-    for (int t = tid; t < L; t += blockDim.x) a.flag[t] = all ? 1 : 0;
+    for (int t = tid; t < L; t += blockDim.x) fl[t] = all ? 1 : 0;
     __syncthreads();
     if (!all && a.mass_thresh > 0.f) {
         // mass to reach, in fixed-point units: ceil(m * T) <= T for m < 1; all
@@ -178,7 +244,7 @@ __global__ void __launch_bounds__(kSelectThreads) k_mass_select(SelectArgs a) {
         const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
         for (int pass = 0; pass < 3; ++pass) {
             const int nbins = 1 << widths[pass];
-            radix_hist<true>(a, nullptr, prefix, pmask, shifts[pass], nbins, scale, hcnt, hmass);
+            radix_hist<true>(sv, L, nullptr, prefix, pmask, shifts[pass], nbins, ex, hcnt, hmass);
             // bins from the top: thread i owns bins nbins-1-2i and nbins-2-2i
             const int b0 = nbins - 1 - 2 * tid, b1 = b0 - 1;
             const unsigned long long m0 = b0 >= 0 ? hmass[b0] : 0ull, m1 = b1 >= 0 ? hmass[b1] : 0ull;
@@ -200,34 +266,34 @@ __global__ void __launch_bounds__(kSelectThreads) k_mass_select(SelectArgs a) {
             __syncthreads();
         }
         const uint32_t cut = prefix;
-        const unsigned long long fq = __double2ull_rn((double)__uint_as_float(cut) * scale);
+        const unsigned long long fq = fixed_mass(__uint_as_float(cut), ex);
         const unsigned long long need = target - above_mass;  // >= 1
         const unsigned long long take = fq ? (need + fq - 1) / fq : 1ull;
         // ordered pass over contiguous segments for the equal keys
         const int seg = (L + blockDim.x - 1) / blockDim.x;
         const int t0 = min(L, tid * seg), t1 = min(L, t0 + seg);
         int eq = 0;
-        for (int t = t0; t < t1; ++t) eq += __float_as_uint(a.s[t]) == cut;
+        for (int t = t0; t < t1; ++t) eq += __float_as_uint(sv[t]) == cut;
         int eqtot;
         const int eqb = block_excl_scan(eq, scr, &eqtot);
         int seen = 0;
         for (int t = t0; t < t1; ++t) {
-            const uint32_t kv = __float_as_uint(a.s[t]);
+            const uint32_t kv = __float_as_uint(sv[t]);
             const bool in = kv > cut || (kv == cut && (unsigned long long)(eqb + seen) < take);
             seen += kv == cut;
-            a.flag[t] = in ? 1 : 0;
+            fl[t] = in ? 1 : 0;
         }
         __syncthreads();
     }
 
     // ---- the last recent_n tokens always run the FFN
     const int tail = a.recent_n < L ? a.recent_n : L;
-    for (int t = L - tail + tid; t < L; t += blockDim.x) a.flag[t] = 1;
+    for (int t = L - tail + tid; t < L; t += blockDim.x) fl[t] = 1;
     __syncthreads();
 
     // ---- at least min(min_keep, L) tokens: extend along (s desc, t asc)
     int cnt_local = 0;
-    for (int t = tid; t < L; t += blockDim.x) cnt_local += a.flag[t];
+    for (int t = tid; t < L; t += blockDim.x) cnt_local += fl[t];
     int nsel;
     block_excl_scan(cnt_local, scr, &nsel);
     const int want = a.min_keep < L ? a.min_keep : L;
@@ -237,7 +303,7 @@ __global__ void __launch_bounds__(kSelectThreads) k_mass_select(SelectArgs a) {
         const int shifts[3] = {21, 10, 0}, widths[3] = {11, 11, 10};
         for (int pass = 0; pass < 3; ++pass) {
             const int nbins = 1 << widths[pass];
-            radix_hist<false>(a, a.flag, prefix, pmask, shifts[pass], nbins, 0.0, hcnt, nullptr);
+            radix_hist<false>(sv, L, fl, prefix, pmask, shifts[pass], nbins, 0, hcnt, nullptr);
             const int b0 = nbins - 1 - 2 * tid, b1 = b0 - 1;
             const unsigned c0 = b0 >= 0 ? hcnt[b0] : 0u, c1 = b1 >= 0 ? hcnt[b1] : 0u;
             int ctot;
@@ -254,16 +320,16 @@ __global__ void __launch_bounds__(kSelectThreads) k_mass_select(SelectArgs a) {
         const int seg = (L + blockDim.x - 1) / blockDim.x;
         const int t0 = min(L, tid * seg), t1 = min(L, t0 + seg);
         int eq = 0;
-        for (int t = t0; t < t1; ++t) eq += !a.flag[t] && __float_as_uint(a.s[t]) == cut;
+        for (int t = t0; t < t1; ++t) eq += !fl[t] && __float_as_uint(sv[t]) == cut;
         int eqtot;
         const int eqb = block_excl_scan(eq, scr, &eqtot);
         int seen = 0;
         for (int t = t0; t < t1; ++t) {  // each thread updates only its own segment
-            if (a.flag[t]) continue;
-            const uint32_t kv = __float_as_uint(a.s[t]);
+            if (fl[t]) continue;
+            const uint32_t kv = __float_as_uint(sv[t]);
             const bool in = kv > cut || (kv == cut && (unsigned)(eqb + seen) < need);
             seen += kv == cut;
-            if (in) a.flag[t] = 1;
+            if (in) fl[t] = 1;
         }
         __syncthreads();
     }
@@ -273,11 +339,11 @@ __global__ void __launch_bounds__(kSelectThreads) k_mass_select(SelectArgs a) {
         const int seg = (L + blockDim.x - 1) / blockDim.x;
         const int t0 = min(L, tid * seg), t1 = min(L, t0 + seg);
         int c = 0;
-        for (int t = t0; t < t1; ++t) c += a.flag[t] != 0;
+        for (int t = t0; t < t1; ++t) c += fl[t] != 0;
         int tot;
         int pos = block_excl_scan(c, scr, &tot);
         for (int t = t0; t < t1; ++t)
-            if (a.flag[t]) a.sel_idx[pos++] = t;
+            if (fl[t]) a.sel_idx[pos++] = t;
         if (tid == 0) a.n_sel[0] = tot;
     }
 }
@@ -316,7 +382,11 @@ sffn_status run_token_select(const void *y_attn, int L, int d, float mass_thresh
     a.flag = reinterpret_cast<uint8_t *>(w + p.off_flag);
     a.sel_idx = sel_idx;
     a.n_sel = n_sel;
-    e = launch_k(k_mass_select, dim3(1), dim3(kSelectThreads), 0, s, a);
+    a.staged = L <= kStageKeys;
+    const size_t smem = a.staged ? (size_t)L * (sizeof(float) + 1) : 0;
+    if (a.staged && set_max_smem((const void *)k_mass_select, (int)(kStageKeys * (sizeof(float) + 1))) != cudaSuccess)
+        return SFFN_ERR_CUDA;
+    e = launch_k(k_mass_select, dim3(1), dim3(kSelectThreads), smem, s, a);
     return e == cudaSuccess ? SFFN_OK : SFFN_ERR_CUDA;
 }
 

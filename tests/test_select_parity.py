@@ -68,7 +68,9 @@ def test_config_prefill_selection_full(sffn, m):
         assert g.size == c["L"]
 
 
-@pytest.mark.parametrize("L", [1, 2, 7, 100, 1023, 1024, 1025, 4099])
+# up to 32768 tokens the importances are staged in shared memory; 40000 takes the
+# workspace path
+@pytest.mark.parametrize("L", [1, 2, 7, 100, 1023, 1024, 1025, 4099, 32768, 40000])
 @pytest.mark.parametrize("m", [0.0, 1e-9, 0.3, 0.9])
 def test_lengths_and_thresholds(sffn, L, m):
     _, ya = W.make_prefill_inputs(L, 64, seed=L)
