@@ -624,13 +624,23 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     if (!a.gbar) return;
 
     // ---- grid barrier: every CTA's partial and chunk counts are written ----
-    // One CTA per SM and grid <= #SMs, so all CTAs are resident; the wait is
-    // bounded all the same.  gbar[0] counts arrivals and is never reset; this
-    // call's barrier opens once it has grown by gridDim.x past the base
+    // Only the first NR CTAs (enough for one 32-column block and four chunk
+    // lists each) finish the call; the others count their arrival and exit at
+    // once, so that the next
+    // call's gate CTAs can take their SMs and start streaming while the output
+    // is formed.  The reducers are resident (one CTA per SM, grid <= #SMs); the
+    // wait is bounded all the same.  gbar[0] counts arrivals and is never reset;
+    // this call's barrier opens once it has grown by gridDim.x past the base
     // (unsigned differences, so wrap-around is harmless).
+    const size_t total = (size_t)a.nb * d;
+    const int NR = (int)min((size_t)gridDim.x, max((total + 31) / 32, (size_t)(gridDim.x + 3) / 4));
     __shared__ int s_bar_ok;
     __threadfence();
     __syncthreads();
+    if ((int)blockIdx.x >= NR) {
+        if (tid == 0) atomicAdd(a.gbar, 1u);
+        return;
+    }
     if (tid == 0) {
         atomicAdd(a.gbar, 1u);
         const volatile unsigned *arrivals = a.gbar;
@@ -653,13 +663,12 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     if (blockIdx.x == 0 && tid == 0) *reinterpret_cast<volatile unsigned *>(a.gbar + 1) = bar_base + gridDim.x;
     if (!s_bar_ok || failed) return;
 
+    const int C = gridDim.x;
     if (warp < 4) {
-        // ---- output: 32-column blocks, partials summed in a fixed order (warp
-        // g adds partials g, g + 4, ...; then the 4 warps in order)
+        // ---- output: 32-column blocks r, r + NR, ...; partials summed in a
+        // fixed order (warp g adds partials g, g + 4, ...; then the 4 warps in order)
         float *red = &sh[0][0];  // [4][32] (sh holds >= 256 floats and is free now)
-        const size_t total = (size_t)a.nb * d;
-        const int C = gridDim.x;
-        for (size_t cb = (size_t)blockIdx.x * 32; cb < total; cb += (size_t)C * 32) {
+        for (size_t cb = (size_t)blockIdx.x * 32; cb < total; cb += (size_t)NR * 32) {
             const size_t col = cb + lane;
             float sum = 0.f;
             if (col < total) {
@@ -684,30 +693,35 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
             named_barrier_sync(1, 128);
         }
     } else {
-        // ---- meanwhile: this chunk's ascending index lists at their global
-        // positions (warp 4 + k takes tokens k, k + 4, ...)
-        for (int b = warp - 4; b < a.nb; b += 4) {
-            const int *cnt = a.cnt + (size_t)b * a.C;
-            // counts of the earlier chunks (C <= kMaxChunks = 256: 8 per lane, in
-            // flight together) and this chunk's entries (R <= 256: 8 per lane)
-            int cv[8], ev[8];
-            const int mine = __ldcg(cnt + blockIdx.x);
+        // ---- meanwhile: the ascending index lists of chunks r, r + NR, ... at
+        // their global positions; warps 4..7 share the (chunk, token) pairs
+        const int nmine_c = ((int)C - (int)blockIdx.x + NR - 1) / NR;
+        for (int q = warp - 4; q < nmine_c * a.nb; q += 4) {
+            const int c = (int)blockIdx.x + (q / a.nb) * NR, b = q % a.nb;
+            const int crow0 = c * a.R;
+            {
+                const int *cnt = a.cnt + (size_t)b * a.C;
+                // counts of the earlier chunks (C <= kMaxChunks = 256: 8 per lane,
+                // in flight together) and the chunk's entries (R <= 256: 8 per lane)
+                int cv[8], ev[8];
+                const int mine = __ldcg(cnt + c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int c = lane + 32 * i, e = lane + 32 * i;
-                cv[i] = c < (int)blockIdx.x ? __ldcg(cnt + c) : 0;
-                ev[i] = e < a.R && row0 + e < F ? __ldcg(a.lidx + (size_t)b * F + row0 + e) : 0;
+                for (int i = 0; i < 8; ++i) {
+                    const int cc = lane + 32 * i, e = lane + 32 * i;
+                    cv[i] = cc < c ? __ldcg(cnt + cc) : 0;
+                    ev[i] = e < a.R && crow0 + e < F ? __ldcg(a.lidx + (size_t)b * F + crow0 + e) : 0;
+                }
+                int sacc = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) sacc += cv[i];
+                const int off = __reduce_add_sync(0xffffffffu, sacc);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < mine) a.active_idx[(size_t)b * F + off + e] = ev[i];
+                }
+                if (c == C - 1 && lane == 0) a.n_active[b] = off + mine;
             }
-            int sacc = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sacc += cv[i];
-            const int off = __reduce_add_sync(0xffffffffu, sacc);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = lane + 32 * i;
-                if (e < mine) a.active_idx[(size_t)b * F + off + e] = ev[i];
-            }
-            if (blockIdx.x == gridDim.x - 1 && lane == 0) a.n_active[b] = off + mine;
         }
     }
 }
