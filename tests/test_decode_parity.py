@@ -192,6 +192,8 @@ BIG_F = [
     (2, 72, 39001, "bf16", "exact", "gate", 3),
     (1, 32, 40960, "f32", "threshold", "gate_up", 2),
     (4, 512, 40000, "int4_g64", "threshold", "gate", 1),
+    (3, 64, 40000, "bf16", "keep_ratio", "gate_up", 1),  # scores beyond the shared-memory stage
+    (3, 64, 40000, "bf16", "keep_ratio", "gate", 2),
 ]
 
 
@@ -201,6 +203,7 @@ def test_more_chunks_than_sms(sffn, case):
     layer = W.make_ffn_layer(cfg, seed=41, d_model=d, d_ff=F, wdtype=wd,
                              act="silu" if wd == "int4_g64" else "relu")
     x = W.make_tokens(cfg, B, seed=9, d_model=d, xdtype="f32" if wd == "f32" else "bf16")
-    tau = _tau_at(layer, x, 0.85, score) if mode == "threshold" else 0.0
-    r = run_and_check_decode(sffn, layer, x, mode, score, tau, nthreads=16)
+    param = {"threshold": lambda: _tau_at(layer, x, 0.85, score), "keep_ratio": lambda: 0.125,
+             "exact": lambda: 0.0}[mode]()
+    r = run_and_check_decode(sffn, layer, x, mode, score, param, nthreads=16)
     assert (r["n_active"] > 0).all()
