@@ -196,13 +196,11 @@ struct GateArgs {
     int act, mode, score_kind;
     float tau;
     int decide;           // 1: exact / threshold decision, lists and h here
-    int list_u;           // list whose entries carry h values (0 if nb == 1, else the union)
     int stages;           // rows in flight per warp (its ring stages)
     float *aeff;          // !decide: [nb, F] raw act values (or null)
     float *uval;          // !decide, UP: [nb, F] u_j (or null)
     float *score;         // [nb, F] or null
     int *cnt, *lidx;      // decide: chunk counts / chunk-local ascending lists
-    float *lh;            // decide: [nb, F] h values aligned with list list_u (unfused only)
     int32_t *err;
     const void *wdT;      // decide: down projection, read for this chunk's active rows
     float *part;          // decide: [C, nb, d] this CTA's fp32 partial of the output
@@ -1377,13 +1375,11 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     ga.score_kind = c.score;
     ga.tau = c.param;
     ga.decide = (!scores_only && !keep) ? 1 : 0;
-    ga.list_u = p.list_u;
     ga.aeff = (keep && !scores_only) ? aeff : nullptr;
     ga.uval = (keep && up && !scores_only) ? uval : nullptr;
     ga.score = scores_only ? c.scores_only : (keep ? score : nullptr);
     ga.cnt = cnt;
     ga.lidx = lidx;
-    ga.lh = lh;
     ga.err = err;
     // exact / threshold with every gate CTA resident: the gate kernel finishes
     // the call itself (grid barrier + distributed reduction + index lists)
