@@ -23,6 +23,8 @@ ACT_RELU, ACT_SILU = 0, 1
 F32, BF16, INT4_G64 = 0, 1, 2
 SCORE_GATE, SCORE_GATE_UP = 0, 1
 WS_DECODE, WS_SELECT, WS_PREFILL = 0, 1, 2
+PRESET_SPEED, PRESET_BALANCED, PRESET_QUALITY, PRESET_DENSE = 0, 1, 2, 3
+_PRESET = {"speed": PRESET_SPEED, "balanced": PRESET_BALANCED, "quality": PRESET_QUALITY, "dense": PRESET_DENSE}
 NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _WDTYPE = {"f32": F32, "bf16": BF16, "int4_g64": INT4_G64}
@@ -40,6 +42,14 @@ class FFNWeights(C.Structure):
                 ("w_gate", C.c_void_p), ("w_up", C.c_void_p), ("w_downT", C.c_void_p),
                 ("s_gate", C.c_void_p), ("s_up", C.c_void_p), ("s_downT", C.c_void_p),
                 ("b_gate", C.c_void_p), ("down_norms", C.c_void_p)]
+
+
+class FFNSchedule(C.Structure):
+    _fields_ = [("dense_until", C.c_int32), ("deep_layer_start", C.c_int32), ("mass_thresh", C.c_float),
+                ("mass_thresh_deep", C.c_float), ("recent_n", C.c_int32), ("min_keep", C.c_int32)]
+
+    def as_dict(self) -> dict:
+        return {k: getattr(self, k) for k, _ in self._fields_}
 
 
 _lib = None
@@ -71,6 +81,15 @@ def lib():
         L.sffn_decode_noalloc.restype = I
         L.sffn_read_device_error.argtypes = [P, C.POINTER(C.c_int32), P]
         L.sffn_read_device_error.restype = I
+        SP = C.POINTER(FFNSchedule)
+        L.sffn_schedule_preset.argtypes = [I, SP]
+        L.sffn_schedule_preset.restype = I
+        L.sffn_schedule_mass.argtypes = [SP, I]
+        L.sffn_schedule_mass.restype = F
+        L.sffn_prefill_layers_workspace_size.argtypes = [I, W]
+        L.sffn_prefill_layers_workspace_size.restype = S
+        L.sffn_prefill_layers.argtypes = [P, C.POINTER(C.c_void_p), I, I, W, SP, I, P, P, P, P, S, P]
+        L.sffn_prefill_layers.restype = I
         _lib = L
     return _lib
 
@@ -223,3 +242,46 @@ def read_device_error(workspace: torch.Tensor, stream=None) -> int:
     _check(lib().sffn_read_device_error(_ptr(workspace), C.byref(code), _stream(stream)),
            "sffn_read_device_error")
     return int(code.value)
+
+
+def schedule_preset(preset) -> FFNSchedule:
+    """One of the presets ("speed", "balanced", "quality", "dense" or its enum)."""
+    s = FFNSchedule()
+    p = _PRESET[preset] if isinstance(preset, str) else int(preset)
+    _check(lib().sffn_schedule_preset(p, C.byref(s)), "sffn_schedule_preset")
+    return s
+
+
+def schedule(dense_until: int, mass_thresh: float, recent_n: int, min_keep: int = 1,
+             deep_layer_start: int = 2**31 - 1, mass_thresh_deep: float | None = None) -> FFNSchedule:
+    return FFNSchedule(int(dense_until), int(deep_layer_start), float(mass_thresh),
+                       float(mass_thresh if mass_thresh_deep is None else mass_thresh_deep), int(recent_n),
+                       int(min_keep))
+
+
+def schedule_mass(s: FFNSchedule, layer: int) -> float:
+    return float(lib().sffn_schedule_mass(C.byref(s), int(layer)))
+
+
+def prefill_layers(x: torch.Tensor, y_attn: list, weights: list, s: FFNSchedule, first_layer: int = 0,
+                   out=None, sel_idx=None, n_sel=None, workspace=None, stream=None):
+    """A stack of token-selective prefill layers; returns (out, sel_idx [n, L], n_sel [n])."""
+    L = x.shape[0]
+    n = len(weights)
+    if out is None:
+        out = torch.empty_like(x)
+    if sel_idx is None:
+        sel_idx = torch.empty((n, L), dtype=torch.int32, device=x.device)
+    if n_sel is None:
+        n_sel = torch.empty(n, dtype=torch.int32, device=x.device)
+    if workspace is None:
+        nb = max(int(lib().sffn_prefill_layers_workspace_size(L, w.ref())) for w in weights)
+        if nb == 0:
+            raise SffnError(ERR_SHAPE, "sffn_prefill_layers_workspace_size")
+        workspace = torch.zeros(nb, dtype=torch.uint8, device=x.device)
+    ya = (C.c_void_p * n)(*[_ptr(t) for t in y_attn])
+    ws = (FFNWeights * n)(*[w.c for w in weights])
+    st = lib().sffn_prefill_layers(_ptr(x), ya, L, n, ws, C.byref(s), int(first_layer), _ptr(out), _ptr(sel_idx),
+                                   _ptr(n_sel), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "sffn_prefill_layers")
+    return out, sel_idx, n_sel

@@ -196,6 +196,64 @@ sffn_status sffn_prefill(const void *x, const void *y_attn, int L, const sffn_ff
                          const int32_t *sel_idx, const int32_t *n_sel, void *out, void *workspace,
                          size_t ws_bytes, sffn_stream_t stream);
 
+/* Per-layer sparsity schedule of a multi-layer token-selective prefill (RedKnot
+ * write-up, the three-tier SparseFFNSchedule):
+ *   layer <  dense_until                       dense FFN (a selection with mass 1:
+ *                                              every token)
+ *   dense_until <= layer < deep_layer_start    select with mass_thresh
+ *   layer >= deep_layer_start                  select with mass_thresh_deep
+ * recent_n and min_keep apply to every layer.  Valid when dense_until >= 0,
+ * deep_layer_start >= 0, both masses >= 0, recent_n >= 0 and min_keep >= 1.
+ * Host struct. */
+typedef struct {
+    int32_t dense_until;
+    int32_t deep_layer_start;
+    float mass_thresh;
+    float mass_thresh_deep;
+    int32_t recent_n;
+    int32_t min_keep;
+} sffn_ffn_schedule;
+
+typedef enum {
+    SFFN_PRESET_SPEED = 0,     /* dense_until 3,  mass 0.3, recent_n 64  */
+    SFFN_PRESET_BALANCED = 1,  /* dense_until 20, mass 0.5, recent_n 128 */
+    SFFN_PRESET_QUALITY = 2,   /* dense_until 32, mass 0.7, recent_n 128 */
+    SFFN_PRESET_DENSE = 3      /* dense_until 80, mass 1.0, recent_n 128 (the dense baseline) */
+} sffn_preset;
+
+/* The write-up's FFN presets table.  The table names no deep tier, so
+ * deep_layer_start = INT32_MAX and mass_thresh_deep = mass_thresh; min_keep = 1.
+ * Returns SFFN_ERR_INVALID_ARG for an unknown preset or out == NULL. */
+sffn_status sffn_schedule_preset(int preset, sffn_ffn_schedule *out);
+
+/* Mass threshold the schedule gives layer `layer` (1 for a dense layer), or a
+ * negative value for an invalid schedule or layer < 0.  Host only. */
+float sffn_schedule_mass(const sffn_ffn_schedule *s, int layer);
+
+/* Workspace bytes for sffn_prefill_layers with L tokens and layers shaped like w
+ * (one selection/prefill region plus one bf16 [L, d_model] buffer); 0 if invalid. */
+size_t sffn_prefill_layers_workspace_size(int L, const sffn_ffn_weights *w);
+
+/* A stack of n_layers token-selective prefill layers, enqueued on `stream`
+ * without a host synchronisation.  Layer i (schedule index first_layer + i)
+ * selects tokens of y_attn[i] with sffn_schedule_mass(s, first_layer + i),
+ * s->recent_n and s->min_keep, then runs sffn_prefill with weights w[i] on the
+ * previous layer's output (x for i = 0).  The last layer's output goes to out.
+ *   x, out      bf16 [L, d_model], distinct buffers.
+ *   y_attn      HOST array of n_layers device pointers, bf16 [L, d_model] each.
+ *   w           HOST array of n_layers weight structs (same d_model; each as
+ *               sffn_prefill requires).
+ *   sel_idx     int32 [n_layers, L]: row i holds layer i's selection; n_sel
+ *               int32 [n_layers].
+ *   workspace   the largest sffn_prefill_layers_workspace_size over the layers
+ *               (zero-filled before first use, like every workspace).
+ * Errors as sffn_token_select / sffn_prefill; SFFN_ERR_SHAPE if the layers'
+ * d_model differ. */
+sffn_status sffn_prefill_layers(const void *x, const void *const *y_attn, int L, int n_layers,
+                                const sffn_ffn_weights *w, const sffn_ffn_schedule *s, int first_layer,
+                                void *out, int32_t *sel_idx, int32_t *n_sel, void *workspace,
+                                size_t ws_bytes, sffn_stream_t stream);
+
 /* Copy the workspace's device error word to *code (host) and clear it; waits
  * for `stream`.  0 = no error; otherwise an sffn_status value. */
 sffn_status sffn_read_device_error(void *workspace, int32_t *code, sffn_stream_t stream);

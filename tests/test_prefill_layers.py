@@ -1,0 +1,71 @@
+"""GPU: a stack of token-selective prefill layers driven by the per-layer
+schedule equals the same layers run one call at a time (bit for bit, selections
+included); the dense tier keeps every token."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+from activation_sparse_ffn_gemv_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sffn():
+    from activation_sparse_ffn_gemv_gb300 import sffn as S
+    S.lib()
+    return S
+
+
+def _stack(sffn, n, L=300, d=256, F=256):
+    layers = [{k: (v.cuda() if torch.is_tensor(v) else v) for k, v in
+               W.make_ffn_layer(5, seed=50 + i, d_model=d, d_ff=F).items()} for i in range(n)]
+    ws = [sffn.Weights(l) for l in layers]
+    X, _ = W.make_prefill_inputs(L, d, seed=1)
+    yas = [W.make_prefill_inputs(L, d, seed=10 + i)[1].cuda() for i in range(n)]
+    return layers, ws, X.cuda(), yas
+
+
+@pytest.mark.parametrize("n,first", [(3, 0), (4, 0), (2, 2)])
+def test_stack_equals_chained_layers(sffn, n, first):
+    layers, ws, x0, yas = _stack(sffn, n)
+    L = x0.shape[0]
+    s = sffn.schedule(dense_until=1, mass_thresh=0.5, recent_n=16, deep_layer_start=3, mass_thresh_deep=0.2)
+    wsp = torch.zeros(max(int(sffn.lib().sffn_prefill_layers_workspace_size(L, w.ref())) for w in ws),
+                      dtype=torch.uint8, device="cuda")
+    out, sel, ns = sffn.prefill_layers(x0, yas, ws, s, first_layer=first, workspace=wsp)
+    x = x0
+    for i in range(n):
+        m = sffn.schedule_mass(s, first + i)
+        si, ni = sffn.token_select(yas[i], m, s.recent_n, s.min_keep)
+        x = sffn.prefill(x, yas[i], ws[i], si, ni)
+        torch.cuda.synchronize()
+        k = int(ni.item())
+        assert int(ns[i].item()) == k, f"layer {first + i}: n_sel"
+        assert torch.equal(sel[i, :k], si[:k]), f"layer {first + i}: selection"
+        if first + i < s.dense_until:
+            assert k == L  # the dense tier keeps every token
+    torch.cuda.synchronize()
+    assert torch.equal(out, x)
+    assert sffn.read_device_error(wsp) == 0
+    # deep layers keep fewer tokens than middle ones at the same inputs' scale
+    masses = [sffn.schedule_mass(s, first + i) for i in range(n)]
+    if 0.2 in [round(m, 3) for m in masses] and 0.5 in [round(m, 3) for m in masses]:
+        nd = [int(ns[i]) for i in range(n) if round(masses[i], 3) == 0.2]
+        nm = [int(ns[i]) for i in range(n) if round(masses[i], 3) == 0.5]
+        assert max(nd) < L and min(nm) < L
+
+
+def test_dense_preset_equals_dense_ffn(sffn):
+    # every layer dense: the stack's output is the chained full-token prefill
+    layers, ws, x0, yas = _stack(sffn, 2)
+    L = x0.shape[0]
+    out, sel, ns = sffn.prefill_layers(x0, yas, ws, sffn.schedule_preset("dense"))
+    all_idx = torch.arange(L, dtype=torch.int32, device="cuda")
+    x = x0
+    for i in range(2):
+        x = sffn.prefill(x, yas[i], ws[i], all_idx, torch.tensor([L], dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert (ns == L).all()
+    assert torch.equal(out, x)
