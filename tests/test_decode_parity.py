@@ -207,3 +207,26 @@ def test_more_chunks_than_sms(sffn, case):
              "exact": lambda: 0.0}[mode]()
     r = run_and_check_decode(sffn, layer, x, mode, score, param, nthreads=16)
     assert (r["n_active"] > 0).all()
+
+
+# Limits of the boundary: one neuron, and the largest d_ff (65536) the decode
+# call accepts (256 chunks of 256 neurons: the unfused finish).
+EDGE = [
+    (2, 64, 1, "bf16", "exact", "gate", 1),
+    (2, 8, 1, "bf16", "exact", "gate", 8),
+    (2, 64, 65536, "bf16", "exact", "gate", 2),
+    (3, 64, 65536, "bf16", "keep_ratio", "gate", 1),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "-".join(map(str, c)))
+def test_edge_shapes(sffn, case):
+    cfg, d, F, wd, mode, score, B = case
+    layer = W.make_ffn_layer(cfg, seed=43, d_model=d, d_ff=F, wdtype=wd)
+    if F == 1:
+        layer["b_gate"] = torch.full((1,), 2.0)  # the single neuron is active for most tokens
+    x = W.make_tokens(cfg, B, seed=11, d_model=d)
+    param = 0.125 if mode == "keep_ratio" else 0.0
+    r = run_and_check_decode(sffn, layer, x, mode, score, param, nthreads=16)
+    if mode == "keep_ratio":
+        assert (r["n_active"] == max(1, int(F * param))).all()
