@@ -5,7 +5,7 @@ Default workload (N=1): Llama-2-7B-shaped ReGLU FFN decode (d_model 4096,
 d_ff 11008, bf16 weights, fp32 accumulation, exact gating, batch 1 token per
 call), 1024 tokens per step rotating over 8 independent layer copies (2.2 GB of
 weights, far larger than L2, so no L2 flush is needed).  A step is one CUDA
-graph of 1024 sffn_decode calls (gate -> sparse up/down -> reduce each).
+graph of 1024 sffn_decode calls (one kernel each at this shape).
 
 Prints one JSON line (rank 0).  `value` is decode microseconds per token over
 all ranks' tokens (lower is better).  The `prefill` object adds the second half
@@ -110,6 +110,23 @@ def dist_setup():
     return ws, rank, local
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum of this rank's timings (ms) over all ranks: the job
+    takes as long as its slowest replica.  Identity without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def per_token_us(ms_max, steps, tokens_per_step, world):
+    """Whole-job microseconds per token: the slowest replica's time over the
+    tokens all replicas processed (weak scaling: each replica runs its own)."""
+    return ms_max * 1e3 / (steps * tokens_per_step * world)
+
+
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
@@ -185,11 +202,7 @@ def run_ours(args):
     barrier()
     clk = clocks.stop() if clocks else None
     ms = e0.elapsed_time(e1)
-    ms_max = ms
-    if dist is not None:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_max = float(t.item())
+    ms_max = max_over_ranks([ms], dist, dev)[0]
 
     # end to end: host buffers in, host buffers out, copies inside the timed region
     xh = x.cpu().pin_memory()
@@ -221,11 +234,7 @@ def run_ours(args):
             nh.copy_(nact, non_blocking=True)
         f1.record(stream)
     f1.synchronize()
-    ms_e2e = f0.elapsed_time(f1)
-    if dist is not None:
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks([f0.elapsed_time(f1)], dist, dev)[0]
 
     # active fraction and algorithmic bytes per token
     n_np = nact.cpu().numpy().astype(np.float64)
@@ -237,7 +246,7 @@ def run_ours(args):
                  + 4.0 * n_np.mean() + 4.0)           # active index list + count
     us_tok = ms_max * 1e3 / (args.steps * T)
     total_tokens = args.steps * T * world
-    value = ms_max * 1e3 / total_tokens
+    value = per_token_us(ms_max, args.steps, T, world)
     hbm, bf16_peak, bf16_sus, peak_src = peaks()
     achieved = bytes_tok / (us_tok * 1e-6) / 1e9
     # one fused kernel per call when every gate chunk's CTA is resident (the
@@ -264,7 +273,7 @@ def run_ours(args):
                          "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(achieved / hbm, 4), "peak_source": peak_src,
                          "bytes_per_launch": round(bytes_tok), "traffic": traffic_for("decode_exact_llama")},
-            "e2e": {"value": round(ms_e2e * 1e3 / total_tokens, 4), "unit": "us/token",
+            "e2e": {"value": round(per_token_us(ms_e2e, args.steps, T, world), 4), "unit": "us/token",
                     "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
                     "d2h_bytes_per_step": int(outh.numel() * outh.element_size() + nh.numel() * 4)},
             "gpu_launches": int(args.steps * T * kernels_per_call),
@@ -554,10 +563,7 @@ def bench_prefill(args, dev, rank, world, dist):
         t_sel = sum(ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(args.prefill_steps)) / args.prefill_steps
         t_ffn = sum(ev[2 * i + 1].elapsed_time(ev[2 * i + 2]) for i in range(args.prefill_steps)) / args.prefill_steps
         t_tot = ev[0].elapsed_time(ev[-1]) / args.prefill_steps
-        if dist is not None:
-            t = torch.tensor([t_tot, t_ffn, t_sel], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            t_tot, t_ffn, t_sel = (float(v) for v in t.tolist())
+        t_tot, t_ffn, t_sel = max_over_ranks([t_tot, t_ffn, t_sel], dist, dev)
         k = int(n.item())
         flops = 6.0 * k * d * F
         tf = flops / (t_ffn * 1e-3) / 1e12
