@@ -13,9 +13,10 @@ code.
 Parity status: every function is pinned by ``tests/test_oracle_pins.py``
 (closed forms, brute force on tiny inputs, numpy fp64 special cases, printed
 worked values from the pages); none is "parity unpinned".  The submodules
-``predictor`` (low-rank gate predictor) and ``tiers`` (keep-ratio tier tables
-with a core set) are pinned by ``tests/test_predictor_oracle.py`` and
-``tests/test_tiers_oracle.py``.
+``predictor`` (low-rank gate predictor), ``tiers`` (keep-ratio tier tables with a
+core set) and ``moe`` (adaptive expert top-K, block token budget) are pinned by
+``tests/test_predictor_oracle.py``, ``tests/test_tiers_oracle.py`` and
+``tests/test_moe_oracle.py``.
 """
 from __future__ import annotations
 
