@@ -47,8 +47,9 @@ int device_smem_optin() {
     return g_smem_optin[dev];
 }
 
+// The attribute is set whatever the size: a kernel's static shared memory
+// counts against the same 48 KB default as its dynamic shared memory.
 cudaError_t set_max_smem(const void *kernel, int bytes) {
-    if (bytes <= 48 * 1024) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -123,6 +124,20 @@ sffn_status check_decode_args(const void *x, int B, const sffn_ffn_weights *w, i
 
 }  // namespace
 
+namespace sffn {
+
+sffn_status validate_decode_call(const void *x, int B, const sffn_ffn_weights *w, int mode, int score, float param,
+                                 const void *out, const int32_t *active_idx, const int32_t *n_active) {
+    sffn_status st = check_decode_args(x, B, w, mode, score, param);
+    if (st != SFFN_OK) return st;
+    if (!out || !active_idx || !n_active) return SFFN_ERR_INVALID_ARG;
+    if (!aligned16(out)) return SFFN_ERR_ALIGNMENT;
+    if (device_sm_count() <= 0) return SFFN_ERR_CUDA;
+    return SFFN_OK;
+}
+
+}  // namespace sffn
+
 extern "C" {
 
 const char *sffn_status_string(sffn_status s) {
@@ -169,11 +184,8 @@ sffn_status sffn_down_norms(const sffn_ffn_weights *w, float *norms, sffn_stream
 sffn_status sffn_decode(const void *x, int B, const sffn_ffn_weights *w, int mode, int score, float param, void *out,
                         int32_t *active_idx, int32_t *n_active, void *workspace, size_t ws_bytes,
                         sffn_stream_t stream) {
-    sffn_status st = check_decode_args(x, B, w, mode, score, param);
+    sffn_status st = validate_decode_call(x, B, w, mode, score, param, out, active_idx, n_active);
     if (st != SFFN_OK) return st;
-    if (!out || !active_idx || !n_active) return SFFN_ERR_INVALID_ARG;
-    if (!aligned16(out)) return SFFN_ERR_ALIGNMENT;
-    if (device_sm_count() <= 0) return SFFN_ERR_CUDA;
     DecodePlan p = make_decode_plan(B, w->d_model, w->d_ff);
     st = check_ws(workspace, ws_bytes, p.total);
     if (st != SFFN_OK) return st;
@@ -252,9 +264,9 @@ sffn_status sffn_read_device_error(void *workspace, int32_t *code, sffn_stream_t
     if (!workspace || !code) return SFFN_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     cudaError_t e = cudaMemcpyAsync(code, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
-    // clears the whole control block: the error word and the decode epoch,
-    // finish count and chunk flags (left mid-count only by a call that recorded
-    // a timeout)
+    // clears the whole control block: the error word and the decode grid
+    // barrier's two counters (left inconsistent only by a call that recorded a
+    // timeout at the barrier)
     if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, kControlBytes, s);
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     return cuda_status(e);

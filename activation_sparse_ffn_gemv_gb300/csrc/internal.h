@@ -65,6 +65,11 @@ struct DecodePlan {
 
 DecodePlan make_decode_plan(int B, int d, int F);
 
+// Every host-side check sffn_decode makes before it looks at the workspace, in
+// the same order and with the same status codes.
+sffn_status validate_decode_call(const void *x, int B, const sffn_ffn_weights *w, int mode, int score, float param,
+                                 const void *out, const int32_t *active_idx, const int32_t *n_active);
+
 struct DecodeCall {
     const void *x;
     const sffn_ffn_weights *w;

@@ -21,7 +21,9 @@ std::mutex g_scratch_mu;
 
 // Device address of g_noalloc_scratch on the current device (looked up on the
 // first call for that device).  Returns nullptr on failure.
-void *scratch_address(int dev) {
+void *scratch_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
     if (g_scratch_addr[dev] == nullptr) {
         void *p = nullptr;
@@ -36,21 +38,31 @@ void *scratch_address(int dev) {
 extern "C" sffn_status sffn_decode_noalloc(const void *x, int B, const sffn_ffn_weights *w, int mode, int score,
                                            float param, void *out, int32_t *active_idx, int32_t *n_active,
                                            sffn_stream_t stream) {
-    // sffn_decode's own validation (it returns before launching anything when
-    // the workspace pointer is null, so check the arguments the same way here).
-    if (!x || !w || !out || !active_idx || !n_active) return SFFN_ERR_INVALID_ARG;
-    size_t need = sffn_workspace_size(0, B, w);
-    if (need == 0) return (B < 1 || B > 8) ? SFFN_ERR_SHAPE : SFFN_ERR_INVALID_ARG;
-    if (need > (size_t)SFFN_NOALLOC_SCRATCH_BYTES) return SFFN_ERR_WORKSPACE;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return SFFN_ERR_CUDA;
-    void *ws = scratch_address(dev);
+    // the same argument checks as sffn_decode, in the same order, before the
+    // shared array is touched
+    sffn_status st = sffn::validate_decode_call(x, B, w, mode, score, param, out, active_idx, n_active);
+    if (st != SFFN_OK) return st;
+    if (sffn::make_decode_plan(B, w->d_model, w->d_ff).total > (size_t)SFFN_NOALLOC_SCRATCH_BYTES)
+        return SFFN_ERR_WORKSPACE;
+    void *ws = scratch_address();
     if (!ws) return SFFN_ERR_CUDA;
-    // The array keeps whatever the previous call left; the decode kernels write
-    // every scratch word before reading it, except the control block (error word,
-    // epoch, finish count, chunk flags), which is cleared here so that each call
-    // starts clean.
-    if (cudaMemsetAsync(ws, 0, sffn::kControlBytes, (cudaStream_t)stream) != cudaSuccess) return SFFN_ERR_CUDA;
+    // The array keeps whatever the previous call left.  The decode kernels write
+    // every scratch word before they read it, except the control block: its
+    // grid-barrier counters (arrivals, and the arrivals before the current call)
+    // are reset here so that each call starts from a consistent pair even after
+    // an earlier call gave up at the barrier.  The error word is left alone: it
+    // keeps the first recorded error until sffn_decode_noalloc_read_error reads
+    // and clears it.
+    cudaError_t e = cudaMemsetAsync(static_cast<char *>(ws) + sffn::kCtlBar, 0, sffn::kControlBytes - sffn::kCtlBar,
+                                    (cudaStream_t)stream);
+    if (e != cudaSuccess) return SFFN_ERR_CUDA;
     return sffn_decode(x, B, w, mode, score, param, out, active_idx, n_active, ws,
                        (size_t)SFFN_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+extern "C" sffn_status sffn_decode_noalloc_read_error(int32_t *code, sffn_stream_t stream) {
+    if (!code) return SFFN_ERR_INVALID_ARG;
+    void *ws = scratch_address();
+    if (!ws) return SFFN_ERR_CUDA;
+    return sffn_read_device_error(ws, code, stream);
 }

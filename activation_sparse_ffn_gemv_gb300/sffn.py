@@ -79,6 +79,8 @@ def lib():
         L.sffn_prefill.restype = I
         L.sffn_decode_noalloc.argtypes = [P, I, W, I, I, F, P, P, P, P]
         L.sffn_decode_noalloc.restype = I
+        L.sffn_decode_noalloc_read_error.argtypes = [C.POINTER(C.c_int32), P]
+        L.sffn_decode_noalloc_read_error.restype = I
         L.sffn_read_device_error.argtypes = [P, C.POINTER(C.c_int32), P]
         L.sffn_read_device_error.restype = I
         SP = C.POINTER(FFNSchedule)
@@ -241,6 +243,13 @@ def read_device_error(workspace: torch.Tensor, stream=None) -> int:
     code = C.c_int32(0)
     _check(lib().sffn_read_device_error(_ptr(workspace), C.byref(code), _stream(stream)),
            "sffn_read_device_error")
+    return int(code.value)
+
+
+def decode_noalloc_read_error(stream=None) -> int:
+    """Device error word of decode_noalloc's built-in array (read and cleared)."""
+    code = C.c_int32(0)
+    _check(lib().sffn_decode_noalloc_read_error(C.byref(code), _stream(stream)), "sffn_decode_noalloc_read_error")
     return int(code.value)
 
 

@@ -158,14 +158,24 @@ sffn_status sffn_decode(const void *x, int B, const sffn_ffn_weights *w, int mod
  *    B <= 2 at d_model 2048 / d_ff 11008.
  *  - The first call on each device looks up the array's device address (with
  *    that device current); make that first call before any stream capture.
+ *  - Argument errors are reported exactly as sffn_decode reports them, before
+ *    anything is enqueued.
  *  - All calls share the one array, which keeps the previous call's contents
- *    (every word is written before it is read; the device error word is
- *    cleared at the start of each call).  Calls that can overlap on the GPU
- *    (different streams, different host threads) race on it: issue them in
- *    one stream order. */
+ *    (every word is written before it is read; the grid-barrier counters are
+ *    reset at the start of each call).  The device error word is not reset by
+ *    a call: it keeps the first error recorded since it was last read with
+ *    sffn_decode_noalloc_read_error.  Calls that can overlap on the GPU
+ *    (different streams, different host threads) race on the array: issue them
+ *    in one stream order. */
 sffn_status sffn_decode_noalloc(const void *x, int B, const sffn_ffn_weights *w, int mode, int score,
                                 float param, void *out, int32_t *active_idx, int32_t *n_active,
                                 sffn_stream_t stream);
+
+/* sffn_read_device_error for the built-in array of sffn_decode_noalloc on the
+ * current device: copies its device error word to *code (host) and clears it,
+ * waiting for `stream`.  0 = no error; SFFN_ERR_TIMEOUT = a bounded wait of an
+ * earlier sffn_decode_noalloc call gave up (its outputs are incomplete). */
+sffn_status sffn_decode_noalloc_read_error(int32_t *code, sffn_stream_t stream);
 
 /* Scores of every neuron for B tokens, fp32 [B, d_ff] (score kind as in
  * sffn_decode; down_norms required).  Reads the gate (and for GATE_UP the up

@@ -59,9 +59,11 @@ def check_outputs(gpu_out: np.ndarray, ref_out: np.ndarray, tol: float):
 
 def run_and_check_decode(sffn, layer_cpu: dict, x_cpu: torch.Tensor, mode: str, score: str = "gate",
                          param: float = 0.0, nthreads: int = 8, out_tol: float | None = None,
-                         batch: int = 8):
+                         batch: int = 8, max_exempt: int | None = None):
     """Runs sffn_decode on the GPU (``batch`` tokens per call) and checks sets +
-    outputs against the oracle."""
+    outputs against the oracle.  At most ``max_exempt`` set elements (default:
+    two per token) may differ inside the tie band: the band only forgives
+    rounding at the cut, so a systematic error near the cut still fails."""
     dev = "cuda"
     layer = layer_to(layer_cpu, dev)
     w = sffn.Weights(layer)
@@ -88,6 +90,8 @@ def run_and_check_decode(sffn, layer_cpu: dict, x_cpu: torch.Tensor, mode: str, 
                    nthreads=nthreads, details=True)
     keep_k = O.keep_count(F, param) if mode == "keep_ratio" else None
     exempt = check_selection(gpu_sets, ref, mode, F, keep_k)
+    limit = 2 * B if max_exempt is None else max_exempt
+    assert exempt <= limit, f"{exempt} set elements differ inside the tie band (limit {limit})"
     err = check_outputs(out.float().cpu().numpy().astype(np.float64), ref["out"],
                         out_tol if out_tol is not None else TOL[layer_cpu["wdtype"]])
     return dict(exempt=exempt, err=err, n_active=n, ref=ref, out=out)

@@ -96,6 +96,34 @@ def test_shape_and_parameter_checks_before_any_cuda_call(S):
     assert L.sffn_workspace_size(5, 1, None) == 0
 
 
+def test_noalloc_reports_argument_errors_like_decode(S):
+    # sffn_decode_noalloc runs sffn_decode's own checks, in the same order, before
+    # it touches its built-in array: every bad argument gives the same status
+    L = S.lib()
+
+    def wts(**kw):
+        f = dict(wdtype=S.BF16, act=S.ACT_RELU, d_model=64, d_ff=128)
+        f.update(kw)
+        return S.FFNWeights(f["wdtype"], f["act"], f["d_model"], f["d_ff"], 16, 16, 16, 16, 16, 16, None, 16)
+
+    cases = [  # (weights, B, mode, score, param, x, out)
+        (wts(d_model=12), 1, 0, 0, 0.0, 16, 16), (wts(d_model=96, wdtype=S.INT4_G64), 1, 0, 0, 0.0, 16, 16),
+        (wts(d_ff=0), 1, 0, 0, 0.0, 16, 16), (wts(d_ff=70000), 1, 0, 0, 0.0, 16, 16),
+        (wts(), 0, 0, 0, 0.0, 16, 16), (wts(), 9, 0, 0, 0.0, 16, 16), (wts(d_model=8192), 1, 0, 0, 0.0, 16, 16),
+        (wts(), 1, 0, 0, 0.0, 8, 16), (wts(), 1, 0, 0, 0.0, 16, 8), (wts(), 1, 2, 0, 0.0, 16, 16),
+        (wts(), 1, 2, 0, 1.5, 16, 16), (wts(), 1, 1, 0, -1.0, 16, 16), (wts(act=5), 1, 0, 0, 0.0, 16, 16),
+        (wts(), 1, 7, 0, 0.0, 16, 16), (wts(), 1, 0, 5, 0.0, 16, 16), (wts(), 1, 0, 0, 0.0, None, 16),
+        (wts(), 1, 0, 0, 0.0, 16, None), (wts(wdtype=S.INT4_G64, d_model=512), 1, 2, 0, 0.5, 16, 16),
+        (wts(wdtype=S.INT4_G64, d_model=576), 1, 0, 0, 0.0, 16, 16),
+    ]
+    for w, B, mode, score, param, x, out in cases:
+        a = L.sffn_decode(x, B, C.byref(w), mode, score, param, out, 16, 16, 256, 1 << 20, None)
+        b = L.sffn_decode_noalloc(x, B, C.byref(w), mode, score, param, out, 16, 16, None)
+        assert a == b and a != S.OK, (a, b)
+    assert L.sffn_decode_noalloc(16, 1, None, 0, 0, 0.0, 16, 16, 16, None) == S.ERR_INVALID_ARG
+    assert L.sffn_decode_noalloc_read_error(None, None) == S.ERR_INVALID_ARG
+
+
 @pytest.mark.gpu
 def test_workspace_checks_on_gpu(S):
     from activation_sparse_ffn_gemv_gb300 import workloads as W

@@ -214,6 +214,50 @@ def test_score_closed_form(act):
     assert np.allclose(r3["out"][0], ref, rtol=1e-15, atol=1e-300)
 
 
+def test_silu_slope_bound_behind_the_tie_band():
+    # The oracle scales the tie band of an activation-based score by 1.1: an
+    # error e in g moves act(g) by at most max|act'| * e.  ReLU's slope is at most
+    # 1; SiLU's, s(z) (1 + z (1 - s(z))), peaks near z = 2.3994 at 1.09984.
+    z = np.linspace(-20.0, 20.0, 4_000_001)
+    sg = 1.0 / (1.0 + np.exp(-z))
+    slope = sg * (1.0 + z * (1.0 - sg))
+    assert 1.0998 < slope.max() < 1.1
+    assert abs(z[slope.argmax()] - 2.3994) < 1e-3
+    assert slope.min() > -0.1   # the negative dip is shallower than the bound too
+
+
+@pytest.mark.parametrize("act", [O.RELU, O.SILU])
+def test_tie_band_conditioning_closed_form(act):
+    # One-hot rows make every dot product a single exact term, so the
+    # conditioning sums are closed forms: cg = |g_j - b_j| + |b_j|, cu = |u_j|.
+    # The bound is tight there (a one-term dot has relative error exactly one
+    # rounding of its only term).  Exact gating: cond = cg.  GATE score:
+    # cond = 1.1 cg n_j.  GATE_UP score: cond = (|u| 1.1 cg + max(|a|, cg) cu) n_j,
+    # the first-order error of |a u| n with a's error bounded through the slope
+    # and max(|a|, cg) covering a near 0.
+    rng = np.random.default_rng(8)
+    F, d = 16, 8
+    g = rng.choice(np.arange(-12, 13), F).astype(np.float32) / 4
+    c = rng.choice([0.25, 0.5, 1.0, 2.0], F).astype(np.float32)
+    u = rng.choice([-3.0, -1.0, 0.5, 2.0], F).astype(np.float32)
+    b = rng.choice([-0.5, 0.0, 0.25], F).astype(np.float32)
+    wg, wu, wd, x = _closed_form_layer(g, c, u, d)
+    ffn = O.FFN(O.Mat(O.F32, wg, F, d), O.Mat(O.F32, wu, F, d), O.Mat(O.F32, wd, F, d), act, torch.from_numpy(b))
+    xm = O.Mat(O.F32, x, 1, d)
+    gg = g.astype(float) + b.astype(float)
+    a = np.maximum(gg, 0.0) if act == O.RELU else gg / (1.0 + np.exp(-gg))
+    cg = np.abs(g.astype(float)) + np.abs(b.astype(float))
+    cu = np.abs(u.astype(float))
+    n = np.abs(c.astype(float))
+    r = O.decode(ffn, xm, O.EXACT, details=True)
+    assert np.array_equal(r["cond"][0], cg)
+    r = O.decode(ffn, xm, O.THRESHOLD, O.SCORE_GATE, 0.0, details=True)
+    assert np.allclose(r["cond"][0], 1.1 * cg * n, rtol=1e-15, atol=0)
+    r = O.decode(ffn, xm, O.THRESHOLD, O.SCORE_GATE_UP, 0.0, details=True)
+    want = (np.abs(u.astype(float)) * 1.1 * cg + np.maximum(np.abs(a), cg) * cu) * n
+    assert np.allclose(r["cond"][0], want, rtol=1e-15, atol=0)
+
+
 def test_keep_ratio_bruteforce_small():
     rng = np.random.default_rng(11)
     for trial in range(30):
