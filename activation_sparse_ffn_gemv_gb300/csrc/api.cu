@@ -206,6 +206,30 @@ sffn_status sffn_decode(const void *x, int B, const sffn_ffn_weights *w, int mod
     return st;
 }
 
+sffn_status sffn_decode_dense(const void *x, int B, const sffn_ffn_weights *w, void *out, void *workspace,
+                              size_t ws_bytes, sffn_stream_t stream) {
+    sffn_status st = check_decode_args(x, B, w, SFFN_MODE_EXACT, SFFN_SCORE_GATE, 0.f);
+    if (st != SFFN_OK) return st;
+    if (!out) return SFFN_ERR_INVALID_ARG;
+    if (!aligned16(out)) return SFFN_ERR_ALIGNMENT;
+    if (w->wdtype != SFFN_BF16 && w->wdtype != SFFN_INT4_G64) return SFFN_ERR_UNSUPPORTED;
+    if (device_sm_count() <= 0) return SFFN_ERR_CUDA;
+    DecodePlan p = make_decode_plan(B, w->d_model, w->d_ff);
+    if (!decode_tc_shape_ok(w, p)) return SFFN_ERR_UNSUPPORTED;
+    st = check_ws(workspace, ws_bytes, p.total);
+    if (st != SFFN_OK) return st;
+    DecodeCall c = {};
+    c.x = x;
+    c.w = w;
+    c.B = B;
+    c.mode = SFFN_MODE_EXACT;
+    c.out = out;
+    c.ws = workspace;
+    st = run_decode_tc(c, p, (cudaStream_t)stream, true);
+    if (st == SFFN_OK) st = cuda_status(cudaGetLastError());
+    return st;
+}
+
 sffn_status sffn_gate_scores(const void *x, int B, const sffn_ffn_weights *w, int score, float *scores,
                              void *workspace, size_t ws_bytes, sffn_stream_t stream) {
     sffn_status st = check_decode_args(x, B, w, SFFN_MODE_THRESHOLD, score, 0.f);

@@ -18,6 +18,7 @@
 // threshold, 2.3 weight-aware score, 3.2 keep-ratio top-k, 3.3 index table
 // instead of a bool mask).
 #include "common.cuh"
+#include "decode_finish.cuh"
 #include "internal.h"
 
 namespace sffn {
@@ -703,108 +704,22 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
         __syncthreads();  // the next batch overwrites the ring
     }
     if (!a.gbar) return;
-
-    // ---- grid barrier: every CTA's partial and chunk counts are written ----
-    // Only the first NR CTAs (enough for one 32-column block and four chunk
-    // lists each) finish the call; the others count their arrival and exit at
-    // once, so that the next
-    // call's gate CTAs can take their SMs and start streaming while the output
-    // is formed.  The reducers are resident (one CTA per SM, grid <= #SMs); the
-    // wait is bounded all the same.  gbar[0] counts arrivals and is never reset;
-    // this call's barrier opens once it has grown by gridDim.x past the base
-    // (unsigned differences, so wrap-around is harmless).
-    const size_t total = (size_t)a.nb * d;
-    const int NR = (int)min((size_t)gridDim.x, max((total + 31) / 32, (size_t)(gridDim.x + 3) / 4));
-    __shared__ int s_bar_ok;
-    __threadfence();
-    __syncthreads();
-    if ((int)blockIdx.x >= NR) {
-        if (tid == 0) atomicAdd(a.gbar, 1u);
-        return;
-    }
-    if (tid == 0) {
-        atomicAdd(a.gbar, 1u);
-        const volatile unsigned *arrivals = a.gbar;
-        int ok = 1;
-        if (*arrivals - bar_base < gridDim.x) {
-            const uint64_t t0 = globaltimer_ns();
-            while (*arrivals - bar_base < gridDim.x)
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    ok = 0;
-                    record_error(a.err, SFFN_ERR_TIMEOUT);
-                    break;
-                }
-        }
-        __threadfence();
-        s_bar_ok = ok;
-    }
-    __syncthreads();
-    // every CTA read the base before it arrived: the next call's base can be
-    // published now (the next call reads it after this grid has completed)
-    if (blockIdx.x == 0 && tid == 0) *reinterpret_cast<volatile unsigned *>(a.gbar + 1) = bar_base + gridDim.x;
-    if (!s_bar_ok || failed) return;
-
-    const int C = gridDim.x;
-    if (warp < 4) {
-        // ---- output: 32-column blocks r, r + NR, ...; partials summed in a
-        // fixed order (warp g adds partials g, g + 4, ...; then the 4 warps in order)
-        float *red = &sh[0][0];  // [4][32] (sh holds >= 256 floats and is free now)
-        for (size_t cb = (size_t)blockIdx.x * 32; cb < total; cb += (size_t)NR * 32) {
-            const size_t col = cb + lane;
-            float sum = 0.f;
-            if (col < total) {
-                // all of this thread's loads in flight at once (C <= 160 in one go)
-                float v[40];
-#pragma unroll
-                for (int i = 0; i < 40; ++i) {
-                    const int pp = warp + 4 * i;
-                    v[i] = pp < C ? __ldcg(a.part + (size_t)pp * total + col) : 0.f;
-                }
-#pragma unroll
-                for (int i = 0; i < 40; ++i) sum += v[i];
-                for (int pp = warp + 160; pp < C; pp += 4) sum += __ldcg(a.part + (size_t)pp * total + col);
-            }
-            red[warp * 32 + lane] = sum;
-            named_barrier_sync(1, 128);
-            if (warp == 0 && col < total) {
-                const float t = ((red[lane] + red[32 + lane]) + red[64 + lane]) + red[96 + lane];
-                if (a.out_f32) static_cast<float *>(a.out)[col] = t;
-                else static_cast<uint16_t *>(a.out)[col] = f32_to_bf16_bits(t);
-            }
-            named_barrier_sync(1, 128);
-        }
-    } else {
-        // ---- meanwhile: the ascending index lists of chunks r, r + NR, ... at
-        // their global positions; warps 4..7 share the (chunk, token) pairs
-        const int nmine_c = ((int)C - (int)blockIdx.x + NR - 1) / NR;
-        for (int q = warp - 4; q < nmine_c * a.nb; q += 4) {
-            const int c = (int)blockIdx.x + (q / a.nb) * NR, b = q % a.nb;
-            const int crow0 = c * a.R;
-            {
-                const int *cnt = a.cnt + (size_t)b * a.C;
-                // counts of the earlier chunks (C <= kMaxChunks = 256: 8 per lane,
-                // in flight together) and the chunk's entries (R <= 256: 8 per lane)
-                int cv[8], ev[8];
-                const int mine = __ldcg(cnt + c);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int cc = lane + 32 * i, e = lane + 32 * i;
-                    cv[i] = cc < c ? __ldcg(cnt + cc) : 0;
-                    ev[i] = e < a.R && crow0 + e < F ? __ldcg(a.lidx + (size_t)b * F + crow0 + e) : 0;
-                }
-                int sacc = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) sacc += cv[i];
-                const int off = __reduce_add_sync(0xffffffffu, sacc);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int e = lane + 32 * i;
-                    if (e < mine) a.active_idx[(size_t)b * F + off + e] = ev[i];
-                }
-                if (c == C - 1 && lane == 0) a.n_active[b] = off + mine;
-            }
-        }
-    }
+    FinishArgs fa;
+    fa.gbar = a.gbar;
+    fa.part = a.part;
+    fa.nb = a.nb;
+    fa.d = d;
+    fa.F = F;
+    fa.C = a.C;
+    fa.R = a.R;
+    fa.cnt = a.cnt;
+    fa.lidx = a.lidx;
+    fa.out = a.out;
+    fa.out_f32 = a.out_f32;
+    fa.active_idx = a.active_idx;
+    fa.n_active = a.n_active;
+    fa.err = a.err;
+    finish_call(fa, bar_base, failed);
 }
 
 // ---------------------------------------------------------------------------
@@ -1597,6 +1512,7 @@ static cudaError_t launch_decode_w(const DecodeCall &c, const DecodePlan &p, cud
 }
 
 sffn_status run_decode(const DecodeCall &c, const DecodePlan &p, cudaStream_t s) {
+    if (decode_tc_eligible(c, p)) return run_decode_tc(c, p, s, false);
     cudaError_t e;
     switch (c.w->wdtype) {
     case SFFN_F32: e = launch_decode_w<WF32>(c, p, s); break;

@@ -1,0 +1,152 @@
+// decode_finish.cuh -- the end of a fused decode call, shared by the decode
+// kernels: a bounded grid barrier over the call's CTAs, then the fixed-order
+// sum of the per-CTA fp32 partials into the output and the per-token ascending
+// lists of active neurons at their global positions.
+#pragma once
+
+#include "common.cuh"
+
+namespace sffn {
+
+struct FinishArgs {
+    unsigned *gbar;       // [2]: arrivals (never reset), arrivals before this call
+    const float *part;    // [gridDim.x, nb, d] fp32 partials, one per CTA
+    int nb, d, F;
+    int C, R;             // chunks (one per CTA) and rows per chunk
+    const int *cnt;       // [nb, C] active rows per chunk, or null (no lists)
+    const int *lidx;      // [nb, F] chunk-local ascending lists at row0 of each chunk
+    void *out;
+    int out_f32;
+    int32_t *active_idx, *n_active;
+    int32_t *err;
+};
+
+// Called by all threads (>= 256) of every CTA of the call once the CTA's
+// partial (and its chunk's counts and lists) are written.  Only the first NR
+// CTAs (enough for one 32-column block and four chunk lists each) finish the
+// call; the others count their arrival and return at once, so that the next
+// call's CTAs can take their SMs while the output is formed.  The reducers are
+// resident (one CTA per SM, grid <= #SMs); the wait is bounded all the same.
+// gbar[0] counts arrivals and is never reset; this call's barrier opens once it
+// has grown by gridDim.x past the base (unsigned differences, so wrap-around is
+// harmless).
+SFFN_DEV void finish_call(const FinishArgs &a, unsigned bar_base, bool failed) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const size_t total = (size_t)a.nb * a.d;
+    const int NR = (int)min((size_t)gridDim.x, max((total + 31) / 32, (size_t)(gridDim.x + 3) / 4));
+    __shared__ int s_bar_ok;
+    __shared__ float red[8][64];
+    __threadfence();
+    __syncthreads();
+    if ((int)blockIdx.x >= NR) {
+        if (tid == 0) atomicAdd(a.gbar, 1u);
+        return;
+    }
+    if (tid == 0) {
+        atomicAdd(a.gbar, 1u);
+        const volatile unsigned *arrivals = a.gbar;
+        int ok = 1;
+        if (*arrivals - bar_base < gridDim.x) {
+            const uint64_t t0 = globaltimer_ns();
+            while (*arrivals - bar_base < gridDim.x)
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    ok = 0;
+                    record_error(a.err, SFFN_ERR_TIMEOUT);
+                    break;
+                }
+        }
+        __threadfence();
+        s_bar_ok = ok;
+    }
+    __syncthreads();
+    // every CTA read the base before it arrived: the next call's base can be
+    // published now (the next call reads it after this grid has completed)
+    if (blockIdx.x == 0 && tid == 0) *reinterpret_cast<volatile unsigned *>(a.gbar + 1) = bar_base + gridDim.x;
+    if (!s_bar_ok || failed) return;
+
+    const int C = gridDim.x;
+    // ---- output: this CTA's 32-column blocks i = 0, 1, 2, ... at columns
+    // (blockIdx.x + NR i) * 32.  Warps 0..3 take the even i, warps 4..7 (after
+    // the lists) the odd i, two blocks per round with all their loads in
+    // flight; the partials are summed in a fixed order (warp w of a group adds
+    // partials w, w + 4, ...; then the group's 4 warps in order).
+    auto reduce = [&](int grp) {
+        const int wl = warp & 3;
+        for (int i = grp; (size_t)(blockIdx.x + (size_t)NR * i) * 32 < total; i += 4) {
+            const size_t colA = (size_t)(blockIdx.x + (size_t)NR * i) * 32 + lane;
+            const size_t colB = (size_t)(blockIdx.x + (size_t)NR * (i + 2)) * 32 + lane;
+            float va[40], vb[40];
+#pragma unroll
+            for (int q = 0; q < 40; ++q) {
+                const int pp = wl + 4 * q;
+                va[q] = (pp < C && colA < total) ? __ldcg(a.part + (size_t)pp * total + colA) : 0.f;
+                vb[q] = (pp < C && colB < total) ? __ldcg(a.part + (size_t)pp * total + colB) : 0.f;
+            }
+            float sa = 0.f, sb = 0.f;
+#pragma unroll
+            for (int q = 0; q < 40; ++q) {
+                sa += va[q];
+                sb += vb[q];
+            }
+            for (int pp = wl + 160; pp < C; pp += 4) {
+                if (colA < total) sa += __ldcg(a.part + (size_t)pp * total + colA);
+                if (colB < total) sb += __ldcg(a.part + (size_t)pp * total + colB);
+            }
+            red[warp][lane] = sa;
+            red[warp][32 + lane] = sb;
+            named_barrier_sync(1 + grp, 128);
+            if (wl == 0) {
+                const int w0 = 4 * grp;
+                const float ta = ((red[w0][lane] + red[w0 + 1][lane]) + red[w0 + 2][lane]) + red[w0 + 3][lane];
+                const float tb = ((red[w0][32 + lane] + red[w0 + 1][32 + lane]) + red[w0 + 2][32 + lane]) +
+                                 red[w0 + 3][32 + lane];
+                if (colA < total) {
+                    if (a.out_f32) static_cast<float *>(a.out)[colA] = ta;
+                    else static_cast<uint16_t *>(a.out)[colA] = f32_to_bf16_bits(ta);
+                }
+                if (colB < total) {
+                    if (a.out_f32) static_cast<float *>(a.out)[colB] = tb;
+                    else static_cast<uint16_t *>(a.out)[colB] = f32_to_bf16_bits(tb);
+                }
+            }
+            named_barrier_sync(1 + grp, 128);
+        }
+    };
+    if (warp < 4) {
+        reduce(0);
+    } else if (warp < 8) {
+        if (a.cnt) {
+            // ---- the ascending index lists of chunks r, r + NR, ... at their
+            // global positions; warps 4..7 share the (chunk, token) pairs
+            const int nmine_c = ((int)C - (int)blockIdx.x + NR - 1) / NR;
+            for (int q = warp - 4; q < nmine_c * a.nb; q += 4) {
+                const int c = (int)blockIdx.x + (q / a.nb) * NR, b = q % a.nb;
+                const int crow0 = c * a.R;
+                const int *cnt = a.cnt + (size_t)b * a.C;
+                // counts of the earlier chunks (C <= 256: 8 per lane, in flight
+                // together) and the chunk's entries (R <= 256: 8 per lane)
+                int cv[8], ev[8];
+                const int mine = __ldcg(cnt + c);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int cc = lane + 32 * i, e = lane + 32 * i;
+                    cv[i] = cc < c ? __ldcg(cnt + cc) : 0;
+                    ev[i] = e < a.R && crow0 + e < a.F ? __ldcg(a.lidx + (size_t)b * a.F + crow0 + e) : 0;
+                }
+                int sacc = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) sacc += cv[i];
+                const int off = __reduce_add_sync(0xffffffffu, sacc);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int e = lane + 32 * i;
+                    if (e < mine) a.active_idx[(size_t)b * a.F + off + e] = ev[i];
+                }
+                if (c == C - 1 && lane == 0) a.n_active[b] = off + mine;
+            }
+        }
+        reduce(1);
+    }
+}
+
+}  // namespace sffn

@@ -82,6 +82,11 @@ struct DecodeCall {
 };
 
 sffn_status run_decode(const DecodeCall &c, const DecodePlan &p, cudaStream_t s);
+// Tensor-core decode (decode_tc.cu): int4-g64 at any B and bf16 with B >= 2,
+// exact or threshold-on-gate-score rules; and the dense layer (dense = true).
+bool decode_tc_shape_ok(const sffn_ffn_weights *w, const DecodePlan &p);
+bool decode_tc_eligible(const DecodeCall &c, const DecodePlan &p);
+sffn_status run_decode_tc(const DecodeCall &c, const DecodePlan &p, cudaStream_t s, bool dense);
 sffn_status run_down_norms(const sffn_ffn_weights *w, float *norms, cudaStream_t s);
 
 // ---------------------------------------------------------------------------

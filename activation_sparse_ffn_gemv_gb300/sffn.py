@@ -71,6 +71,8 @@ def lib():
         L.sffn_down_norms.restype = I
         L.sffn_decode.argtypes = [P, I, W, I, I, F, P, P, P, P, S, P]
         L.sffn_decode.restype = I
+        L.sffn_decode_dense.argtypes = [P, I, W, P, P, S, P]
+        L.sffn_decode_dense.restype = I
         L.sffn_gate_scores.argtypes = [P, I, W, I, P, P, S, P]
         L.sffn_gate_scores.restype = I
         L.sffn_token_select.argtypes = [P, I, I, F, I, I, P, P, P, S, P]
@@ -178,6 +180,18 @@ def decode(x: torch.Tensor, w: Weights, mode: int, score: int = SCORE_GATE, para
                            _stream(stream))
     _check(st, "sffn_decode")
     return out, active_idx, n_active
+
+
+def decode_dense(x: torch.Tensor, w: Weights, out=None, workspace=None, stream=None):
+    """The dense layer (every neuron): out [B, d]."""
+    B = x.shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    if workspace is None:
+        workspace = alloc_workspace(WS_DECODE, B, w, x.device)
+    st = lib().sffn_decode_dense(_ptr(x), B, w.ref(), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "sffn_decode_dense")
+    return out
 
 
 def decode_noalloc(x: torch.Tensor, w: Weights, mode: int, score: int = SCORE_GATE, param: float = 0.0,

@@ -137,6 +137,16 @@ sffn_status sffn_decode(const void *x, int B, const sffn_ffn_weights *w, int mod
                         float param, void *out, int32_t *active_idx, int32_t *n_active,
                         void *workspace, size_t ws_bytes, sffn_stream_t stream);
 
+/* The dense layer, nothing skipped: out = W_down (act(W_gate x + b) (.) (W_up x))
+ * over every neuron, the baseline that denseflux sec. 5.3 measures the sparse
+ * layer against (breakeven active fraction, speedup at 10% active).  Reads all
+ * three matrices once; no index lists.  x, out: bf16 [B, d_model]; weights bf16
+ * or int4-g64; workspace as sffn_decode's (sffn_workspace_size(0, B, w)).
+ * Needs d_model % 512 == 0, d_model <= 4096 and d_ff <= 128 * (#SMs); other
+ * shapes and fp32 weights return SFFN_ERR_UNSUPPORTED. */
+sffn_status sffn_decode_dense(const void *x, int B, const sffn_ffn_weights *w, void *out, void *workspace,
+                              size_t ws_bytes, sffn_stream_t stream);
+
 /* Size of the scratch array built into the library for sffn_decode_noalloc. */
 #define SFFN_NOALLOC_SCRATCH_BYTES (4u << 20)
 

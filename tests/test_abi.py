@@ -124,6 +124,26 @@ def test_noalloc_reports_argument_errors_like_decode(S):
     assert L.sffn_decode_noalloc_read_error(None, None) == S.ERR_INVALID_ARG
 
 
+def test_dense_layer_argument_checks(S):
+    L = S.lib()
+
+    def wts(**kw):
+        f = dict(wdtype=S.BF16, act=S.ACT_RELU, d_model=512, d_ff=128)
+        f.update(kw)
+        return S.FFNWeights(f["wdtype"], f["act"], f["d_model"], f["d_ff"], 16, 16, 16, 16, 16, 16, None, None)
+
+    def dense(w, B=1, x=16, out=16):
+        return L.sffn_decode_dense(x, B, C.byref(w), out, 256, 1 << 20, None)
+
+    assert dense(wts(), x=None) == S.ERR_INVALID_ARG
+    assert dense(wts(), out=None) == S.ERR_INVALID_ARG
+    assert dense(wts(), out=8) == S.ERR_ALIGNMENT
+    assert dense(wts(), B=9) == S.ERR_SHAPE
+    assert dense(wts(wdtype=S.F32)) == S.ERR_UNSUPPORTED
+    assert dense(wts(d_model=8192)) == S.ERR_SHAPE
+    assert L.sffn_decode_dense(16, 1, None, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+
+
 @pytest.mark.gpu
 def test_workspace_checks_on_gpu(S):
     from activation_sparse_ffn_gemv_gb300 import workloads as W

@@ -230,3 +230,60 @@ def test_edge_shapes(sffn, case):
     r = run_and_check_decode(sffn, layer, x, mode, score, param, nthreads=16)
     if mode == "keep_ratio":
         assert (r["n_active"] == max(1, int(F * param))).all()
+
+
+# The tensor-core path (int4 at any token count, bf16 with 2..8 tokens) at the
+# full configuration shapes, and the dense layer (every neuron) it is measured
+# against.
+
+@pytest.mark.parametrize("B", [2, 4, 8])
+def test_config_qwen_int4_threshold_batched(sffn, B):
+    layer = W.make_ffn_layer(4, seed=0, layer=20 + B)
+    x = W.make_tokens(4, B, seed=20 + B)
+    tau = _tau_at(layer, x, 0.9)
+    r = run_and_check_decode(sffn, layer, x, "threshold", "gate", tau, nthreads=16)
+    assert abs(r["n_active"].mean() / layer["d_ff"] - 0.1) < 0.02
+
+
+@pytest.mark.parametrize("B", [2, 4])
+def test_config_llama_reglu_batched(sffn, B):
+    layer = W.make_ffn_layer(2, seed=0, layer=B)
+    x = W.make_tokens(2, B, seed=30 + B)
+    r = run_and_check_decode(sffn, layer, x, "exact", nthreads=16)
+    assert abs(r["n_active"].mean() / layer["d_ff"] - 0.125) < 0.02
+
+
+def test_int4_exact_relu_small_chunks(sffn):
+    # int4 weights with ReLU gating and a bias; ragged last tile of each chunk
+    d, F = 1024, 1500
+    layer = W.make_ffn_layer(4, seed=35, d_model=d, d_ff=F, act="relu")
+    layer["b_gate"] = torch.full((F,), -0.05)
+    x = W.make_tokens(4, 3, seed=35, d_model=d)
+    r = run_and_check_decode(sffn, layer, x, "exact")
+    assert (r["n_active"] > 0).all() and (r["n_active"] < F).all()
+
+
+DENSE = [
+    # (cfg, d, F, wdtype, act, B)
+    (4, 2048, 11008, "int4_g64", "silu", 1),
+    (4, 1024, 700, "int4_g64", "silu", 3),
+    (2, 4096, 11008, "bf16", "relu", 1),
+    (3, 1024, 2050, "bf16", "silu", 8),
+]
+
+
+@pytest.mark.parametrize("case", DENSE, ids=lambda c: "-".join(map(str, c)))
+def test_dense_layer_matches_oracle(sffn, case):
+    from tests.oracle_io import ffn_from_layer, mat_from_act
+    from tests.parity import TOL, check_outputs, layer_to
+    import oracle as O
+    cfg, d, F, wd, act, B = case
+    layer = W.make_ffn_layer(cfg, seed=71, d_model=d, d_ff=F, wdtype=wd, act=act)
+    x = W.make_tokens(cfg, B, seed=71, d_model=d)
+    w = sffn.Weights(layer_to(layer, "cuda"))
+    out = sffn.decode_dense(x.cuda(), w)
+    torch.cuda.synchronize()
+    # threshold 0 on the gate score keeps every neuron: the dense FFN (pinned)
+    ref = O.decode(ffn_from_layer(layer), mat_from_act(x), O.THRESHOLD, O.SCORE_GATE, 0.0, nthreads=16)
+    assert (ref["n_active"] == F).all()
+    check_outputs(out.float().cpu().numpy().astype(np.float64), ref["out"], TOL[wd])
