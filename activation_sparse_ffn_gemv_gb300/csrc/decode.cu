@@ -173,26 +173,21 @@ __global__ void __launch_bounds__(256) k_down_norms(const void *wdT, const void 
 // ---------------------------------------------------------------------------
 //
 // One CTA per SM owns R consecutive neurons (a "chunk").  Warp w of the CTA
-// owns a contiguous block of about R / 8 rows of the chunk and streams it
-// through its own ring of D shared-memory stages: one ring item is up to RPI
-// consecutive rows (RPI = 8 KB / row bytes, at most 8), moved by one bulk copy
-// of their weights (and one of their int4 group scales), completing on one
-// mbarrier per stage.  Few large copies matter on this part: a bulk copy has a
-// fixed issue cost per SM, so rows of 1 KB must not travel one by one.  Against
-// x held in registers the warp forms the gate dot products (and, for the
-// gate-and-up score, the up dot products), then bias, act, score and the
-// decision.  For the exact and threshold rules the item the warp queues after
-// a gate item with active rows carries those rows' W_up rows (consecutive
-// active rows in one copy), so u_j and h_j = a_j u_j are known when the gate
-// stream ends; the active neurons' W_downT rows are prefetched into L2 at the
-// decision.  After the stream each CTA compacts its chunk into ascending
-// per-token lists, bulk-loads its active W_downT rows into the idle ring
-// (consecutive rows in one copy) and accumulates its fp32 partial of the
-// output.  When all CTAs are resident (grid <= #SMs) they then meet at a
-// bounded grid barrier, sum 32-column blocks of the partials in a fixed order
-// and write their chunk's lists; otherwise k_reduce does that.  Every wait is
-// time-bounded; on a timeout the CTA records SFFN_ERR_TIMEOUT, lets its own
-// copies in flight land and skips the rest of its work.
+// streams rows w, w + 8, w + 16, ... of the chunk through its own ring of D
+// shared-memory stages (1-D bulk copies issued by its lane 0, one mbarrier per
+// stage) and forms the gate dot products (and, for the gate-and-up score, the
+// up dot products) against x held in registers, then bias, act, score and the
+// decision.  For the exact and threshold rules the item the warp puts into its
+// ring after an active row is that neuron's W_up row, so u_j and h_j = a_j u_j
+// are known when the gate stream ends; the neuron's W_downT row is prefetched
+// into L2 at the decision.  After the stream each CTA compacts its chunk into
+// ascending per-token lists, bulk-loads its active W_downT rows into the idle
+// ring and accumulates its fp32 partial of the output.  When all CTAs are
+// resident (grid <= #SMs) they then meet at a bounded grid barrier, sum
+// 32-column blocks of the partials in a fixed order and write their chunk's
+// lists; otherwise k_reduce does that.  Every wait is time-bounded; on a
+// timeout the CTA records SFFN_ERR_TIMEOUT, lets its own copies in flight land
+// and skips the rest of its work.
 
 struct GateArgs {
     const void *wg, *wu;
@@ -202,8 +197,7 @@ struct GateArgs {
     int act, mode, score_kind;
     float tau;
     int decide;           // 1: exact / threshold decision, lists and h here
-    int stages;           // items in flight per warp (its ring stages)
-    int rpi;              // rows per ring item
+    int stages;           // rows in flight per warp (its ring stages)
     float *aeff;          // !decide: [nb, F] raw act values (or null)
     float *uval;          // !decide, UP: [nb, F] u_j (or null)
     float *score;         // [nb, F] or null
@@ -225,41 +219,20 @@ constexpr int kGateThreads = 32 * kGateWarps;
 constexpr int kMaxChunk = 256;   // R <= kMaxChunk <= blockDim: one scan pass compacts a chunk
 constexpr int kMaxStages = 16;   // ring stages per warp
 constexpr int kMaxChunks = 256;  // C <= kMaxChunks <= blockDim: one scan pass over the chunk counts
-constexpr int kMaxRpi = 8;       // rows per ring item
-constexpr uint32_t kItemBytes = 8192;  // target weight bytes of one ring item
-
-// A ring item in one word: its first row within the chunk (bits 0..8), its row
-// count (bits 9..12), and for an up item the mask of its rows whose W_up row it
-// carries (bits 13..20) and the up flag (bit 21).
-constexpr int kItemUp = 1 << 21;
-SFFN_HOST_DEV int item_gate(int r0, int cnt) { return r0 | (cnt << 9); }
-SFFN_HOST_DEV int item_up(int r0, int cnt, unsigned mask) { return r0 | (cnt << 9) | (int)(mask << 13) | kItemUp; }
-SFFN_HOST_DEV int item_r0(int it) { return it & 0x1ff; }
-SFFN_HOST_DEV int item_cnt(int it) { return (it >> 9) & 0xf; }
-SFFN_HOST_DEV unsigned item_mask(int it) { return ((unsigned)it >> 13) & 0xffu; }
-
-// Rows per ring item for a given stored row size.
-SFFN_HOST_DEV int rows_per_item(uint32_t row_bytes) {
-    const uint32_t r = kItemBytes / row_bytes;
-    return r < 1 ? 1 : (r > (uint32_t)kMaxRpi ? kMaxRpi : (int)r);
-}
+constexpr int kUpItem = 1 << 16; // ring item tag: the W_up row of the neuron in the low bits
 
 // Bytes of the gate kernel's mbarrier block (one per stage, one for the active
 // rows' copies after the stream), 128-byte aligned.
 SFFN_HOST_DEV uint32_t gate_bar_bytes(int D) { return ((uint32_t)((kGateWarps * D + 1) * 8) + 127u) & ~127u; }
 
-// Length of the run of set bits of m starting at bit i.
-SFFN_DEV int run_from(unsigned m, int i) { return __ffs(~(m >> i)) - 1; }
-
 // Dot products of one stored row (and, with TWO, a second row) with the nb
 // tokens' activations: each lane takes units lane, lane + 32, ... (d_model <=
-// 4096), four independent accumulators per token and row.  sa / sb point at
-// the rows' group scales (int4).  x comes from registers (xr, one token) or
-// shared memory (xs).
+// 4096), four independent accumulators per token and row.  x comes from
+// registers (xr, one token) or shared memory (xs).
 template <class W, int NB, bool TWO, bool XREG>
-SFFN_DEV void row_dots(const unsigned char *ra, const unsigned char *sa_row, const unsigned char *rb,
-                       const unsigned char *sb_row, uint32_t units, const float *xr, const uint4 *xs,
-                       uint32_t xunits, float (&acca)[NB][4], float (&accb)[NB][4]) {
+SFFN_DEV void row_dots(const unsigned char *ra, const unsigned char *rb, uint32_t units, uint32_t row_bytes,
+                       const float *xr, const uint4 *xs, uint32_t xunits, float (&acca)[NB][4],
+                       float (&accb)[NB][4]) {
     constexpr int UPL = 128 / W::E;         // units per lane at d_model <= 4096
     constexpr int CU = W::E >= 32 ? 1 : 4;  // units loaded together (ILP)
     const int lane = threadIdx.x & 31;
@@ -276,10 +249,10 @@ SFFN_DEV void row_dots(const unsigned char *ra, const unsigned char *sa_row, con
             const uint32_t u = (i0 + c) * 32 + lane;
             const bool in = u < units;
             va[c] = in ? *reinterpret_cast<const uint4 *>(ra + u * 16) : make_uint4(0, 0, 0, 0);
-            sa[c] = W::Q && in ? W::scale_at(sa_row, u) : 1.f;
+            sa[c] = W::Q && in ? W::scale_at(ra + row_bytes, u) : 1.f;
             if (TWO) {
                 vb[c] = in ? *reinterpret_cast<const uint4 *>(rb + u * 16) : make_uint4(0, 0, 0, 0);
-                sb[c] = W::Q && in ? W::scale_at(sb_row, u) : 1.f;
+                sb[c] = W::Q && in ? W::scale_at(rb + row_bytes, u) : 1.f;
             }
         }
 #pragma unroll
@@ -342,27 +315,6 @@ SFFN_DEV void row_dots(const unsigned char *ra, const unsigned char *sa_row, con
     }
 }
 
-// Eight consecutive columns (v * 8 ..) of a stored row, dequantised: the
-// down-projection accumulation owns columns in groups of eight.
-template <class W>
-SFFN_DEV void load8(const unsigned char *row, const unsigned char *srow, int v, float *f);
-template <>
-SFFN_DEV void load8<WF32>(const unsigned char *row, const unsigned char *, int v, float *f) {
-    WF32::unpack(*reinterpret_cast<const uint4 *>(row + v * 32), f);
-    WF32::unpack(*reinterpret_cast<const uint4 *>(row + v * 32 + 16), f + 4);
-}
-template <>
-SFFN_DEV void load8<WBF16>(const unsigned char *row, const unsigned char *, int v, float *f) {
-    WBF16::unpack(*reinterpret_cast<const uint4 *>(row + v * 16), f);
-}
-template <>
-SFFN_DEV void load8<WINT4>(const unsigned char *row, const unsigned char *srow, int v, float *f) {
-    const uint32_t w = *reinterpret_cast<const uint32_t *>(row + v * 4) ^ 0x88888888u;
-    const float s = WINT4::scale_at(srow, (uint32_t)(v >> 2));  // group of column 8v: unit v / 4
-#pragma unroll
-    for (int k = 0; k < 8; ++k) f[k] = (__uint_as_float(0x4B000000u | ((w >> (4 * k)) & 0xFu)) - 8388616.0f) * s;
-}
-
 template <class W, int NB, bool UP>
 __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     extern __shared__ __align__(128) unsigned char smraw[];
@@ -370,12 +322,8 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     const uint32_t units = (uint32_t)(d / W::E);  // 16-byte units per row
     const uint32_t row_bytes = units * 16u;
     const uint32_t sbytes = W::Q ? (uint32_t)(d / 64) * 2u : 0u;  // group scales of one row
-    const uint32_t rspace = row_bytes + sbytes;
-    const int rpi = a.rpi;
-    // a stage: [rpi rows of codes][their scales] (+ the same for the up rows)
-    const uint32_t part_bytes = (uint32_t)rpi * rspace;
-    const uint32_t stage_bytes = UP ? 2u * part_bytes : part_bytes;
-    const uint32_t scl_off = (uint32_t)rpi * row_bytes;  // scales within a part
+    const uint32_t rspace = row_bytes + sbytes;    // a row (codes, then scales) in shared memory
+    const uint32_t stage_bytes = UP ? 2u * rspace : rspace;
     const uint32_t xunits = (uint32_t)(d * (int)sizeof(typename W::X) / 16);
     const int D = a.stages;                        // stages (items in flight) per warp
     // dynamic shared memory: [warps][D] + 1 mbarriers | [warps][D] stages | x
@@ -383,27 +331,19 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     uint64_t *dbar = full + (size_t)kGateWarps * D;  // active-row copies after the stream
     const uint32_t bar_bytes = gate_bar_bytes(D);
     unsigned char *ring = smraw + bar_bytes;
-    const size_t ring_bytes = (size_t)kGateWarps * D * stage_bytes;
-    unsigned char *xraw = ring + ring_bytes;
+    unsigned char *xraw = ring + (size_t)kGateWarps * D * stage_bytes;
     const uint4 *xs = reinterpret_cast<const uint4 *>(xraw);   // x in its own dtype [NB][d]
-    __shared__ int sitem[kGateWarps][kMaxStages];  // the item in each stage
+    __shared__ int sitem[kGateWarps][kMaxStages];  // item in each stage: row, | kUpItem for its W_up row
     __shared__ uint8_t sflag[kMaxChunk];
     __shared__ float sh[kMaxChunk][NB];
     __shared__ float sbias[kMaxChunk], snorm[kMaxChunk];
-    __shared__ int scan_tmp[34];
     __shared__ volatile int s_abort;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int row0 = blockIdx.x * a.R;
     const int nrows = min(a.R, F - row0);
-    // warp w owns rows [wr0, wr1) of the chunk, split into ngi gate items
-    const int wr0 = (warp * nrows) / kGateWarps, wr1 = ((warp + 1) * nrows) / kGateWarps;
-    const int nmine = wr1 - wr0;
-    const int ngi = (nmine + rpi - 1) / rpi;
-    auto gate_item = [&](int g) {
-        const int r0 = wr0 + (g * nmine) / ngi, r1 = wr0 + ((g + 1) * nmine) / ngi;
-        return item_gate(r0, r1 - r0);
-    };
+    // warp w handles rows w, w + 8, w + 16, ... of the chunk
+    const int nmine = nrows > warp ? (nrows - warp + kGateWarps - 1) / kGateWarps : 0;
     const bool up_items = a.decide && !UP;  // W_up rows of active neurons join the stream
     uint64_t *wfull = full + (size_t)warp * D;
     unsigned char *wring = ring + (size_t)warp * D * stage_bytes;
@@ -413,47 +353,38 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     const char *gsbase = W::Q ? static_cast<const char *>(a.sg) + (size_t)row0 * sbytes : nullptr;
     const char *usbase = W::Q ? static_cast<const char *>(a.su) + (size_t)row0 * sbytes : nullptr;
     uint64_t pol = 0;
-    // Put item `it` into stage s (lane 0): a gate item's rows (codes, then
-    // scales; then the same of the up rows for the gate-and-up score), or an up
-    // item's masked W_up rows at their places, consecutive rows in one copy.
+    // Put item `it` into stage s (lane 0): gate row codes [+ scales] [+ up row
+    // codes [+ scales]], or one W_up row for an up item.
     auto issue = [&](int s, int it) {
         unsigned char *stage = wring + (size_t)s * stage_bytes;
         uint64_t *bar = &wfull[s];
-        const int r0 = item_r0(it), cnt = item_cnt(it);
+        const size_t r = (size_t)(it & (kUpItem - 1));
         witem[s] = it;
-        if (it & kItemUp) {
-            unsigned m = item_mask(it);
-            mbar_arrive_expect_tx(bar, (uint32_t)__popc(m) * rspace);
-            while (m) {
-                const int i = __ffs(m) - 1, n = run_from(m, i);
-                const size_t r = (size_t)(r0 + i);
-                bulk_load(stage + (size_t)i * row_bytes, ubase + r * row_bytes, (uint32_t)n * row_bytes, bar, pol);
-                if (W::Q)
-                    bulk_load(stage + scl_off + (size_t)i * sbytes, usbase + r * sbytes, (uint32_t)n * sbytes, bar, pol);
-                m &= ~(((1u << n) - 1u) << i);
-            }
+        if (it & kUpItem) {
+            mbar_arrive_expect_tx(bar, rspace);
+            bulk_load(stage, ubase + r * row_bytes, row_bytes, bar, pol);
+            if (W::Q) bulk_load(stage + row_bytes, usbase + r * sbytes, sbytes, bar, pol);
             return;
         }
-        mbar_arrive_expect_tx(bar, (UP ? 2u : 1u) * (uint32_t)cnt * rspace);
-        bulk_load(stage, gbase + (size_t)r0 * row_bytes, (uint32_t)cnt * row_bytes, bar, pol);
-        if (W::Q) bulk_load(stage + scl_off, gsbase + (size_t)r0 * sbytes, (uint32_t)cnt * sbytes, bar, pol);
+        mbar_arrive_expect_tx(bar, stage_bytes);
+        bulk_load(stage, gbase + r * row_bytes, row_bytes, bar, pol);
+        if (W::Q) bulk_load(stage + row_bytes, gsbase + r * sbytes, sbytes, bar, pol);
         if (UP) {
-            bulk_load(stage + part_bytes, ubase + (size_t)r0 * row_bytes, (uint32_t)cnt * row_bytes, bar, pol);
-            if (W::Q)
-                bulk_load(stage + part_bytes + scl_off, usbase + (size_t)r0 * sbytes, (uint32_t)cnt * sbytes, bar, pol);
+            bulk_load(stage + rspace, ubase + r * row_bytes, row_bytes, bar, pol);
+            if (W::Q) bulk_load(stage + rspace + row_bytes, usbase + r * sbytes, sbytes, bar, pol);
         }
     };
     // Each warp keeps its own D items in flight and re-issues as soon as it has
     // consumed one: no producer warp, so a slow warp never holds back another
     // warp's stream.  Item i always sits in stage i % D.  Weights are constant
     // inputs: they stream before the dependency wait.
-    int issued = min(D, ngi);  // items issued by this warp (warp-uniform)
-    int gnext = issued;        // gate items issued
+    int issued = min(D, nmine);  // items issued by this warp (warp-uniform)
+    int gnext = issued;          // gate rows issued: the warp's rows 0 .. gnext-1
     if (lane == 0) {
         for (int i = 0; i < D; ++i) mbar_init(&wfull[i], 1);
         mbar_fence_init();
         pol = l2_evict_first_policy();
-        for (int i = 0; i < issued; ++i) issue(i, gate_item(i));
+        for (int i = 0; i < issued; ++i) issue(i, warp + i * kGateWarps);
     }
     if (tid == 0) {
         s_abort = 0;
@@ -519,96 +450,86 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
                 break;
             }
             const int it = witem[si];
-            const int r0 = item_r0(it), cnt = item_cnt(it);
+            const int r = it & (kUpItem - 1);
             const unsigned char *st = wring + (size_t)si * stage_bytes;
             int next = -1;  // the item that goes into the ring after this one
-            if (it & kItemUp) {
-                // W_up rows of active neurons: u_j per token, h_j = a_j u_j
-                unsigned m = item_mask(it);
-                while (m) {
-                    const int i = __ffs(m) - 1;
-                    m &= m - 1;
-                    const int r = r0 + i;
-                    float acu[NB][4], unused[NB][4];
-                    row_dots<W, NB, false, XREG>(st + (size_t)i * row_bytes, st + scl_off + (size_t)i * sbytes,
-                                                 nullptr, nullptr, units, xr, xs, xunits, acu, unused);
-                    float uu = 0.f;
-#pragma unroll
-                    for (int b = 0; b < NB; ++b) {
-                        const float t = warp_sum((acu[b][0] + acu[b][1]) + (acu[b][2] + acu[b][3]));
-                        if (lane == b) uu = t;
-                    }
-                    if (lane < a.nb) sh[r][lane] = ((sflag[r] >> lane) & 1u) ? sh[r][lane] * uu : 0.f;
+            if (it & kUpItem) {
+                // W_up row of an active neuron: u_j per token, h_j = a_j u_j
+                float acu[NB][4], unused[NB][4];
+                row_dots<W, NB, false, XREG>(st, nullptr, units, row_bytes, xr, xs, xunits, acu, unused);
+                __syncwarp();
+                if (gnext < nmine) next = warp + (gnext++) * kGateWarps;
+                if (lane == 0 && next >= 0) {
+                    fence_proxy_async_smem();
+                    issue(issued % D, next);
                 }
-                __syncwarp();  // every lane is done with the stage
-                if (gnext < ngi) next = gate_item(gnext++);
+                float uu = 0.f;
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    const float t = warp_sum((acu[b][0] + acu[b][1]) + (acu[b][2] + acu[b][3]));
+                    if (lane == b) uu = t;
+                }
+                if (lane < a.nb) sh[r][lane] = ((sflag[r] >> lane) & 1u) ? sh[r][lane] * uu : 0.f;
+                if (next >= 0) ++issued;
+                continue;
+            }
+            float accg[NB][4], accu[NB][4];
+            row_dots<W, NB, UP, XREG>(st, st + rspace, units, row_bytes, xr, xs, xunits, accg, accu);
+            __syncwarp();
+            if (!up_items) {
+                // stage consumed: refill it now with this warp's next gate row
+                if (gnext < nmine) next = warp + (gnext++) * kGateWarps;
                 if (lane == 0 && next >= 0) {
                     fence_proxy_async_smem();
                     issue(issued % D, next);
                 }
                 if (next >= 0) ++issued;
-                continue;
             }
-            unsigned amask = 0u;  // rows of this item active for some token
-            for (int i = 0; i < cnt; ++i) {
-                const int r = r0 + i;
-                float accg[NB][4], accu[NB][4];
-                const unsigned char *pg = st + (size_t)i * row_bytes;
-                row_dots<W, NB, UP, XREG>(pg, st + scl_off + (size_t)i * sbytes, pg + part_bytes,
-                                          st + part_bytes + scl_off + (size_t)i * sbytes, units, xr, xs, xunits,
-                                          accg, accu);
-                float g = 0.f, uu = 0.f;
+            float g = 0.f, uu = 0.f;
 #pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    const float sg = warp_sum((accg[b][0] + accg[b][1]) + (accg[b][2] + accg[b][3]));
-                    const float su = UP ? warp_sum((accu[b][0] + accu[b][1]) + (accu[b][2] + accu[b][3])) : 0.f;
-                    if (lane == b) { g = sg; uu = su; }
-                }
-                const int j = row0 + r;
-                bool active = false;
-                float av = 0.f;
-                if (lane < a.nb) {
-                    g += sbias[r];
-                    av = act_fn(a.act, g);
-                    float sc = 0.f;
-                    if (a.score || (a.decide && a.mode != SFFN_MODE_EXACT)) {
-                        sc = (a.score_kind == SFFN_SCORE_GATE_UP ? fabsf(av * uu) : fabsf(av)) * snorm[r];
-                        if (a.score) a.score[(size_t)lane * F + j] = sc;
-                    }
-                    if (a.decide) {
-                        active = a.mode == SFFN_MODE_EXACT ? av != 0.f : sc >= a.tau;
-                    } else {
-                        if (a.aeff) a.aeff[(size_t)lane * F + j] = av;
-                        if (UP && a.uval) a.uval[(size_t)lane * F + j] = uu;
-                    }
-                }
-                if (!a.decide) continue;
-                const unsigned m = __ballot_sync(0xffffffffu, active) & 0xffu;
-                // UP: h_j = a_j u_j now; otherwise the masked a_j, times u_j when
-                // the item with the W_up row arrives
-                if (lane < NB) sh[r][lane] = active ? (UP ? av * uu : av) : 0.f;
-                if (lane == 0) sflag[r] = (uint8_t)m;
-                if (m != 0u) amask |= 1u << i;
+            for (int b = 0; b < NB; ++b) {
+                const float sg = warp_sum((accg[b][0] + accg[b][1]) + (accg[b][2] + accg[b][3]));
+                const float su = UP ? warp_sum((accu[b][0] + accu[b][1]) + (accu[b][2] + accu[b][3])) : 0.f;
+                if (lane == b) { g = sg; uu = su; }
             }
-            __syncwarp();  // every lane is done with the stage; sh / sflag written
-            if (up_items && amask != 0u) next = item_up(r0, cnt, amask);
-            else if (gnext < ngi) next = gate_item(gnext++);
-            if (lane == 0) {
-                if (next >= 0) {
+            const int j = row0 + r;
+            bool active = false;
+            float av = 0.f;
+            if (lane < a.nb) {
+                g += sbias[r];
+                av = act_fn(a.act, g);
+                float sc = 0.f;
+                if (a.score || (a.decide && a.mode != SFFN_MODE_EXACT)) {
+                    sc = (a.score_kind == SFFN_SCORE_GATE_UP ? fabsf(av * uu) : fabsf(av)) * snorm[r];
+                    if (a.score) a.score[(size_t)lane * F + j] = sc;
+                }
+                if (a.decide) {
+                    active = a.mode == SFFN_MODE_EXACT ? av != 0.f : sc >= a.tau;
+                } else {
+                    if (a.aeff) a.aeff[(size_t)lane * F + j] = av;
+                    if (UP && a.uval) a.uval[(size_t)lane * F + j] = uu;
+                }
+            }
+            if (!a.decide) continue;
+            const unsigned m = __ballot_sync(0xffffffffu, active) & 0xffu;
+            // UP: h_j = a_j u_j now; otherwise the masked a_j, times u_j when the
+            // W_up row (the next item) arrives
+            if (lane < NB) sh[r][lane] = active ? (UP ? av * uu : av) : 0.f;
+            if (lane == 0) sflag[r] = (uint8_t)m;
+            if (up_items) {
+                if (m != 0u) next = r | kUpItem;
+                else if (gnext < nmine) next = warp + (gnext++) * kGateWarps;
+                if (lane == 0 && next >= 0) {
                     fence_proxy_async_smem();
                     issue(issued % D, next);
                 }
-                // the active neurons' W_downT rows, wanted after the stream
-                unsigned m = amask;
-                while (m) {
-                    const int i = __ffs(m) - 1, n = run_from(m, i);
-                    const size_t j = (size_t)(row0 + r0 + i);
-                    bulk_prefetch_l2(static_cast<const char *>(a.wdT) + j * row_bytes, (uint32_t)n * row_bytes);
-                    if (W::Q) bulk_prefetch_l2(static_cast<const char *>(a.sd) + j * sbytes, (uint32_t)n * sbytes);
-                    m &= ~(((1u << n) - 1u) << i);
-                }
+                if (next >= 0) ++issued;
             }
-            if (next >= 0) ++issued;
+            if (m != 0u && lane == 0) {
+                bulk_prefetch_l2(static_cast<const char *>(a.wdT) + (size_t)j * row_bytes, row_bytes);
+                if (W::Q) bulk_prefetch_l2(static_cast<const char *>(a.sd) + (size_t)j * sbytes, sbytes);
+            }
+            __syncwarp();  // sh / sflag of this row before a later up item of the warp reads them
         }
     }
     __syncthreads();
@@ -619,52 +540,62 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
 
     // ordered compaction of this chunk: one list per token for the active_idx
     // output, and (in shared memory) the chunk's rows active for any token
+    // (row r = tid; R <= 256: one ballot per warp and list, one pass)
     __shared__ int sdown[kMaxChunk];
     __shared__ int s_ndown;
+    __shared__ int wcnt[NB + 1][kGateWarps];
     const uint32_t m = tid < nrows ? sflag[tid] : 0u;
-    for (int l = 0; l < a.nb; ++l) {
-        const int p = (int)((m >> l) & 1u);
-        int total;
-        const int pos = block_excl_scan(p, scan_tmp, &total);
-        if (p) a.lidx[(size_t)l * F + row0 + pos] = row0 + tid;
-        if (tid == 0) a.cnt[(size_t)l * a.C + blockIdx.x] = total;
+    for (int l = 0; l <= a.nb; ++l) {
+        const bool bit = l < a.nb ? ((m >> l) & 1u) : m != 0u;
+        const unsigned bl = __ballot_sync(0xffffffffu, bit);
+        if (lane == 0) wcnt[l][warp] = __popc(bl);
     }
+    __syncthreads();
     {
-        const int p = m != 0u;
-        int total;
-        const int pos = block_excl_scan(p, scan_tmp, &total);
-        if (p) sdown[pos] = tid;
-        if (tid == 0) s_ndown = total;
+        const unsigned lt = (1u << lane) - 1u;
+        for (int l = 0; l <= a.nb; ++l) {
+            const bool bit = l < a.nb ? ((m >> l) & 1u) : m != 0u;
+            const unsigned bl = __ballot_sync(0xffffffffu, bit);
+            int base = 0, tot = 0;
+#pragma unroll
+            for (int w = 0; w < kGateWarps; ++w) {
+                base += w < warp ? wcnt[l][w] : 0;
+                tot += wcnt[l][w];
+            }
+            const int pos = base + __popc(bl & lt);
+            if (bit) {
+                if (l < a.nb) a.lidx[(size_t)l * F + row0 + pos] = row0 + tid;
+                else sdown[pos] = tid;
+            }
+            if (tid == 0) {
+                if (l < a.nb) a.cnt[(size_t)l * a.C + blockIdx.x] = tot;
+                else s_ndown = tot;
+            }
+        }
     }
     __syncthreads();
 
     // Active neurons of this chunk (h_j already known), in batches that fit the
     // idle ring: their W_downT rows come from L2 (prefetched at the decision) by
-    // bulk copy in one round trip, laid out [codes of the batch][their scales];
-    // then every thread owns groups of 8 output columns and accumulates
-    // h_j * W_down[:, j] over the rows in ascending order (deterministic) into
-    // this CTA's partial.
+    // bulk copy in one round trip; then every thread owns 16-byte column units
+    // and accumulates h_j * W_down[:, j] over the rows in ascending order
+    // (deterministic) into this CTA's partial.
     const int ndown = failed ? 0 : s_ndown;
-    const int cap = (int)(ring_bytes / rspace);
+    const int cap = (int)((size_t)kGateWarps * D * stage_bytes / rspace);
     const char *wd = static_cast<const char *>(a.wdT);
     const char *sd = static_cast<const char *>(a.sd);
     for (int b0 = 0, batch = 0;; b0 += cap, ++batch) {
         const int bn = min(cap, ndown - b0);
-        const unsigned char *dscl = ring + (size_t)(bn > 0 ? bn : 0) * row_bytes;
         if (bn > 0) {
             if (tid == 0) {
                 fence_proxy_async_smem();  // earlier generic reads of the ring precede the copies
                 const uint64_t pol = l2_evict_first_policy();
                 mbar_arrive_expect_tx(dbar, (uint32_t)bn * rspace);
-                for (int i = 0; i < bn;) {
-                    int n = 1;
-                    while (i + n < bn && sdown[b0 + i + n] == sdown[b0 + i] + n) ++n;
+                for (int i = 0; i < bn; ++i) {
                     const size_t j = (size_t)(row0 + sdown[b0 + i]);
-                    bulk_load(ring + (size_t)i * row_bytes, wd + j * row_bytes, (uint32_t)n * row_bytes, dbar, pol);
-                    if (W::Q)
-                        bulk_load(ring + (size_t)bn * row_bytes + (size_t)i * sbytes, sd + j * sbytes,
-                                  (uint32_t)n * sbytes, dbar, pol);
-                    i += n;
+                    unsigned char *dslot = ring + (size_t)i * rspace;
+                    bulk_load(dslot, wd + j * row_bytes, row_bytes, dbar, pol);
+                    if (W::Q) bulk_load(dslot + row_bytes, sd + j * sbytes, sbytes, dbar, pol);
                 }
             }
             const bool ok = mbar_wait(dbar, (uint32_t)batch & 1u);
@@ -674,29 +605,30 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
                 break;
             }
         }
-        for (int v = tid; v < d / 8; v += blockDim.x) {
+        for (uint32_t u = tid; u < units; u += blockDim.x) {
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 if (b >= a.nb) break;
-                float acc[8];
+                float acc[W::E];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+                for (int e = 0; e < W::E; ++e) acc[e] = 0.f;
                 for (int i = 0; i < bn; ++i) {
                     const float h = sh[sdown[b0 + i]][b];
-                    float f[8];
-                    load8<W>(ring + (size_t)i * row_bytes, dscl + (size_t)i * sbytes, v, f);
+                    const unsigned char *dr = ring + (size_t)i * rspace;
+                    float f[W::E];
+                    W::dequant(*reinterpret_cast<const uint4 *>(dr + u * 16), W::Q ? W::scale_at(dr + row_bytes, u) : 1.f, f);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(h, f[e], acc[e]);
+                    for (int e = 0; e < W::E; ++e) acc[e] = fmaf(h, f[e], acc[e]);
                 }
-                float4 *dst = reinterpret_cast<float4 *>(a.part + ((size_t)blockIdx.x * a.nb + b) * d + (size_t)v * 8);
+                float4 *dst = reinterpret_cast<float4 *>(a.part + ((size_t)blockIdx.x * a.nb + b) * d + u * W::E);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    float4 t = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                for (int q = 0; q < W::E / 4; ++q) {
+                    float4 v = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
                     if (batch > 0) {
                         const float4 o = dst[q];
-                        t.x += o.x; t.y += o.y; t.z += o.z; t.w += o.w;
+                        v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
                     }
-                    dst[q] = t;
+                    dst[q] = v;
                 }
             }
         }
@@ -705,20 +637,9 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     }
     if (!a.gbar) return;
     FinishArgs fa;
-    fa.gbar = a.gbar;
-    fa.part = a.part;
-    fa.nb = a.nb;
-    fa.d = d;
-    fa.F = F;
-    fa.C = a.C;
-    fa.R = a.R;
-    fa.cnt = a.cnt;
-    fa.lidx = a.lidx;
-    fa.out = a.out;
-    fa.out_f32 = a.out_f32;
-    fa.active_idx = a.active_idx;
-    fa.n_active = a.n_active;
-    fa.err = a.err;
+    fa.gbar = a.gbar; fa.part = a.part; fa.nb = a.nb; fa.d = d; fa.F = F; fa.C = a.C; fa.R = a.R;
+    fa.cnt = a.cnt; fa.lidx = a.lidx; fa.out = a.out; fa.out_f32 = a.out_f32; fa.active_idx = a.active_idx;
+    fa.n_active = a.n_active; fa.err = a.err;
     finish_call(fa, bar_base, failed);
 }
 
@@ -1266,14 +1187,15 @@ __global__ void __launch_bounds__(256) k_reduce(ReduceArgs a) {
     __syncthreads();
     const int *lidx = a.lidx + (size_t)b * a.F;
     int32_t *dst = a.active_idx + (size_t)b * a.F;
+    // (a count or offset outside the token's list is never written)
     for (int c = c0 + wp; c < c1; c += blockDim.x >> 5) {
         const int n = ccnt[c - c0], o = coffs[c - c0];
-        if (n <= 128)
+        if (n >= 0 && n <= 128 && o >= 0 && o + n <= a.F)
             for (int i = lane; i < n; i += 32) dst[o + i] = lidx[(size_t)c * a.R + i];
     }
     for (int c = c0; c < c1; ++c) {  // long lists (keep-ratio: the whole list sits in chunk 0)
         const int n = ccnt[c - c0], o = coffs[c - c0];
-        if (n > 128)
+        if (n > 128 && o >= 0 && o + n <= a.F)
             for (int i = tid; i < n; i += blockDim.x) dst[o + i] = lidx[(size_t)c * a.R + i];
     }
 }
@@ -1322,22 +1244,18 @@ static cudaError_t launch_gate(const GateArgs &ga_in, const DecodePlan &p, cudaS
     GateArgs ga = ga_in;
     const uint32_t row_bytes = (uint32_t)(p.d / W::E) * 16u;
     const uint32_t sbytes = W::Q ? (uint32_t)(p.d / 64) * 2u : 0u;
-    const int rows_per_warp = (p.R + kGateWarps - 1) / kGateWarps;
-    const int rpi = min(rows_per_item(row_bytes), rows_per_warp);
-    const uint32_t stage_bytes = (UP ? 2u : 1u) * (uint32_t)rpi * (row_bytes + sbytes);
+    const uint32_t stage_bytes = (UP ? 2u : 1u) * (row_bytes + sbytes);
     const size_t x_bytes = (size_t)NB * p.d * sizeof(typename W::X);
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, (const void *)k_gate<W, NB, UP>);
     if (e != cudaSuccess) return e;
     const long avail = (long)device_smem_optin() - (long)fa.sharedSizeBytes - 1024 - (long)x_bytes - 16;
     long D = avail / ((long)kGateWarps * (stage_bytes + sizeof(uint64_t)));
-    if (D > kMaxStages) D = kMaxStages;
-    // a warp's whole share of the chunk can be in flight: no more stages than gate items
-    const int items_per_warp = (rows_per_warp + rpi - 1) / rpi;
-    if (D > items_per_warp) D = items_per_warp;
+    if (D > 16) D = 16;  // small rows: a warp's whole share of the chunk can be in flight
+    const int rows_per_warp = (p.R + kGateWarps - 1) / kGateWarps;
+    if (D > rows_per_warp) D = rows_per_warp;
     if (D < 1) return cudaErrorInvalidConfiguration;
     ga.stages = (int)D;
-    ga.rpi = rpi;
     const size_t smem = gate_smem(x_bytes, stage_bytes, ga.stages);
     e = set_max_smem((const void *)k_gate<W, NB, UP>, (int)smem);
     if (e != cudaSuccess) return e;

@@ -35,7 +35,7 @@ SFFN_DEV void finish_call(const FinishArgs &a, unsigned bar_base, bool failed) {
     const size_t total = (size_t)a.nb * a.d;
     const int NR = (int)min((size_t)gridDim.x, max((total + 31) / 32, (size_t)(gridDim.x + 3) / 4));
     __shared__ int s_bar_ok;
-    __shared__ float red[8][64];
+    __shared__ float red[8][32];
     __threadfence();
     __syncthreads();
     if ((int)blockIdx.x >= NR) {
@@ -67,47 +67,32 @@ SFFN_DEV void finish_call(const FinishArgs &a, unsigned bar_base, bool failed) {
     const int C = gridDim.x;
     // ---- output: this CTA's 32-column blocks i = 0, 1, 2, ... at columns
     // (blockIdx.x + NR i) * 32.  Warps 0..3 take the even i, warps 4..7 (after
-    // the lists) the odd i, two blocks per round with all their loads in
-    // flight; the partials are summed in a fixed order (warp w of a group adds
-    // partials w, w + 4, ...; then the group's 4 warps in order).
+    // the lists) the odd i; within a group the partials are summed in a fixed
+    // order (warp w of the group adds partials w, w + 4, ... with all its loads
+    // in flight at once; then the group's 4 warps in order).
     auto reduce = [&](int grp) {
         const int wl = warp & 3;
-        for (int i = grp; (size_t)(blockIdx.x + (size_t)NR * i) * 32 < total; i += 4) {
-            const size_t colA = (size_t)(blockIdx.x + (size_t)NR * i) * 32 + lane;
-            const size_t colB = (size_t)(blockIdx.x + (size_t)NR * (i + 2)) * 32 + lane;
-            float va[40], vb[40];
+        for (int i = grp; (size_t)(blockIdx.x + (size_t)NR * i) * 32 < total; i += 2) {
+            const size_t col = (size_t)(blockIdx.x + (size_t)NR * i) * 32 + lane;
+            float sum = 0.f;
+            if (col < total) {
+                float v[40];
 #pragma unroll
-            for (int q = 0; q < 40; ++q) {
-                const int pp = wl + 4 * q;
-                va[q] = (pp < C && colA < total) ? __ldcg(a.part + (size_t)pp * total + colA) : 0.f;
-                vb[q] = (pp < C && colB < total) ? __ldcg(a.part + (size_t)pp * total + colB) : 0.f;
-            }
-            float sa = 0.f, sb = 0.f;
+                for (int q = 0; q < 40; ++q) {
+                    const int pp = wl + 4 * q;
+                    v[q] = pp < C ? __ldcg(a.part + (size_t)pp * total + col) : 0.f;
+                }
 #pragma unroll
-            for (int q = 0; q < 40; ++q) {
-                sa += va[q];
-                sb += vb[q];
+                for (int q = 0; q < 40; ++q) sum += v[q];
+                for (int pp = wl + 160; pp < C; pp += 4) sum += __ldcg(a.part + (size_t)pp * total + col);
             }
-            for (int pp = wl + 160; pp < C; pp += 4) {
-                if (colA < total) sa += __ldcg(a.part + (size_t)pp * total + colA);
-                if (colB < total) sb += __ldcg(a.part + (size_t)pp * total + colB);
-            }
-            red[warp][lane] = sa;
-            red[warp][32 + lane] = sb;
+            red[warp][lane] = sum;
             named_barrier_sync(1 + grp, 128);
-            if (wl == 0) {
+            if (wl == 0 && col < total) {
                 const int w0 = 4 * grp;
-                const float ta = ((red[w0][lane] + red[w0 + 1][lane]) + red[w0 + 2][lane]) + red[w0 + 3][lane];
-                const float tb = ((red[w0][32 + lane] + red[w0 + 1][32 + lane]) + red[w0 + 2][32 + lane]) +
-                                 red[w0 + 3][32 + lane];
-                if (colA < total) {
-                    if (a.out_f32) static_cast<float *>(a.out)[colA] = ta;
-                    else static_cast<uint16_t *>(a.out)[colA] = f32_to_bf16_bits(ta);
-                }
-                if (colB < total) {
-                    if (a.out_f32) static_cast<float *>(a.out)[colB] = tb;
-                    else static_cast<uint16_t *>(a.out)[colB] = f32_to_bf16_bits(tb);
-                }
+                const float t = ((red[w0][lane] + red[w0 + 1][lane]) + red[w0 + 2][lane]) + red[w0 + 3][lane];
+                if (a.out_f32) static_cast<float *>(a.out)[col] = t;
+                else static_cast<uint16_t *>(a.out)[col] = f32_to_bf16_bits(t);
             }
             named_barrier_sync(1 + grp, 128);
         }
@@ -125,18 +110,27 @@ SFFN_DEV void finish_call(const FinishArgs &a, unsigned bar_base, bool failed) {
                 const int *cnt = a.cnt + (size_t)b * a.C;
                 // counts of the earlier chunks (C <= 256: 8 per lane, in flight
                 // together) and the chunk's entries (R <= 256: 8 per lane)
+                // A count outside [0, R] or a list that would end past d_ff means the
+                // control block was not a valid start (e.g. not zero-filled before
+                // first use, so the barrier opened early): record it, write nothing.
                 int cv[8], ev[8];
                 const int mine = __ldcg(cnt + c);
+                int bad = mine < 0 || mine > a.R;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int cc = lane + 32 * i, e = lane + 32 * i;
                     cv[i] = cc < c ? __ldcg(cnt + cc) : 0;
+                    bad |= cv[i] < 0 || cv[i] > a.R;
                     ev[i] = e < a.R && crow0 + e < a.F ? __ldcg(a.lidx + (size_t)b * a.F + crow0 + e) : 0;
                 }
                 int sacc = 0;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) sacc += cv[i];
                 const int off = __reduce_add_sync(0xffffffffu, sacc);
+                if (__any_sync(0xffffffffu, bad) || off < 0 || off + mine > a.F) {
+                    if (lane == 0) record_error(a.err, SFFN_ERR_DEVICE);
+                    continue;
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int e = lane + 32 * i;

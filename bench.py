@@ -158,6 +158,9 @@ def run_ours(args):
     nact = torch.empty(T, dtype=torch.int32, device=dev)
     work = sffn.alloc_workspace(sffn.WS_DECODE, 1, ws_list[0], dev)
     stream = torch.cuda.Stream(device=dev)
+    # the inputs and the zero-filled workspace are made on the default stream:
+    # they must be complete before the decode stream uses them
+    torch.cuda.synchronize()
 
     def enqueue(xin, oo):
         for t in range(T):
@@ -275,7 +278,8 @@ def run_ours(args):
                          "bytes_per_launch": round(bytes_tok), "traffic": traffic_for("decode_exact_llama")},
             "e2e": {"value": round(per_token_us(ms_e2e, args.steps, T, world), 4), "unit": "us/token",
                     "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
-                    "d2h_bytes_per_step": int(outh.numel() * outh.element_size() + nh.numel() * 4)},
+                    "d2h_bytes_per_step": int(outh.numel() * outh.element_size() + nh.numel() * 4),
+                    "copied": "x in; out and n_active back; the active_idx lists stay on the device"},
             "gpu_launches": int(args.steps * T * kernels_per_call),
             "clocks": clk,
         }
@@ -336,9 +340,12 @@ def _time_graph(enqueue, stream, steps, warmup):
 
 
 def bench_decode_sweeps(args, dev, T=256):
-    """The other decode workloads: int4 active-fraction sweep with breakeven,
-    keep-ratio tiers, batched tokens, the tiny fp32 layer.  Each point is a
-    CUDA graph of T single-call decodes rotating over the workload's layers."""
+    """The other decode workloads.  Each point is a CUDA graph of T decode calls
+    rotating over the workload's layers (far more weight bytes than L2):
+    the int4 active-fraction sweep against the dense layer (speed-ups and the
+    breakeven active fraction), batched tokens on the Llama shape, keep-ratio
+    tiers (both scores) and the tiny fp32 layer.  Each point reports microseconds
+    per token and its HBM roofline fraction on the bytes the call must read."""
     import numpy as np
     import torch
 
@@ -352,106 +359,128 @@ def bench_decode_sweeps(args, dev, T=256):
         d = c["d_model"]
         return {"f32": 4.0 * d, "bf16": 2.0 * d, "int4_g64": d / 2 + 2.0 * d / 64}[c["wdtype"]]
 
-    def run_points(cfgn, nl, points, B=1):
-        """points: list of (mode, score, param_per_layer); returns us/token, mean active fraction."""
-        c = W.CONFIGS[cfgn]
+    def point(us, nbytes, **kw):
+        gbps = nbytes / (us * 1e-6) / 1e9
+        return dict(us_per_token=round(us, 3), gbps=round(gbps, 1), frac_hbm=round(gbps / hbm, 4), **kw)
+
+    def setup(cfgn, nl, B=1, norms=True):
         layers = [W.make_ffn_layer(cfgn, seed=100, layer=l, device=dev) for l in range(nl)]
         ws = [sffn.Weights(L) for L in layers]
-        for w in ws:
-            w.set_down_norms(sffn.down_norms(w))
+        if norms:
+            for w in ws:
+                w.set_down_norms(sffn.down_norms(w))
         x = W.make_tokens(cfgn, T * B, seed=5, device=dev)
-        F = c["d_ff"]
-        o = torch.empty_like(x)
-        idx = torch.empty((T * B, F), dtype=torch.int32, device=dev)
-        n = torch.empty(T * B, dtype=torch.int32, device=dev)
-        work = sffn.alloc_workspace(sffn.WS_DECODE, B, ws[0], dev)
-        res = []
-        for mode, score, params in points:
-            def enq():
-                for t in range(T):
-                    sl = slice(t * B, (t + 1) * B)
-                    sffn.decode(x[sl], ws[t % nl], mode, score, params[t % nl], out=o[sl], active_idx=idx[sl],
-                                n_active=n[sl], workspace=work, stream=stream)
-            ms = _time_graph(enq, stream, max(3, args.steps // 3), args.warmup)
-            res.append((ms * 1e3 / (T * B), float(n.float().mean().item()) / F))
-        return c, layers, ws, x, res
+        F = ws[0].d_ff
+        bufs = dict(o=torch.empty_like(x), idx=torch.empty((T * B, F), dtype=torch.int32, device=dev),
+                    n=torch.empty(T * B, dtype=torch.int32, device=dev),
+                    work=sffn.alloc_workspace(sffn.WS_DECODE, B, ws[0], dev))
+        torch.cuda.synchronize()  # made on the default stream, used on `stream`
+        return layers, ws, x, bufs
 
-    # int4 sweep: threshold tau_a = (1 - a) quantile of the layer's gate scores
+    def run_sparse(ws, x, bufs, B, mode, score, params):
+        nl = len(ws)
+
+        def enq():
+            for t in range(T):
+                sl = slice(t * B, (t + 1) * B)
+                sffn.decode(x[sl], ws[t % nl], mode, score, params[t % nl], out=bufs["o"][sl],
+                            active_idx=bufs["idx"][sl], n_active=bufs["n"][sl], workspace=bufs["work"],
+                            stream=stream)
+        return _time_graph(enq, stream, max(3, args.steps // 3), args.warmup) * 1e3 / T
+
+    def run_dense(ws, x, bufs, B):
+        nl = len(ws)
+
+        def enq():
+            for t in range(T):
+                sl = slice(t * B, (t + 1) * B)
+                sffn.decode_dense(x[sl], ws[t % nl], out=bufs["o"][sl], workspace=bufs["work"], stream=stream)
+        return _time_graph(enq, stream, max(3, args.steps // 3), args.warmup) * 1e3 / T
+
+    # ---- int4 sweep: threshold tau_a = (1 - a) quantile of the layer's gate scores
     c = W.CONFIGS[4]
     nl = c["layers"]
-    layers = [W.make_ffn_layer(4, seed=100, layer=l, device=dev) for l in range(nl)]
-    ws = [sffn.Weights(L) for L in layers]
-    for w in ws:
-        w.set_down_norms(sffn.down_norms(w))
+    layers, ws, x, bufs = setup(4, nl)
     calib = W.make_tokens(4, 256, seed=77, device=dev)
     sc_ws = sffn.alloc_workspace(sffn.WS_DECODE, 8, ws[0], dev)
-    taus = {}
-    for l, w in enumerate(ws):
-        sc = torch.cat([sffn.gate_scores(calib[i:i + 8], w, sffn.SCORE_GATE, workspace=sc_ws) for i in range(0, 256, 8)])
-        q = torch.quantile(sc.flatten()[::4].float(), torch.tensor([1.0 - a for a in c["sweep_a"]], device=dev))
-        taus[l] = q.tolist()
-    del layers, ws, sc_ws
-    pts = [(sffn.MODE_THRESHOLD, sffn.SCORE_GATE, [taus[l][i] if c["sweep_a"][i] < 1.0 else 0.0 for l in range(nl)])
-           for i in range(len(c["sweep_a"]))]
-    # dense reference: every neuron (tau = 0 on the gate-and-up score keeps all), the
-    # gate and up rows streamed together and every W_downT row read: the dense FFN
-    # bytes (3 matrices) through the same kernels, without the skip
-    pts.append((sffn.MODE_THRESHOLD, sffn.SCORE_GATE_UP, [0.0] * nl))
-    cfg, _, _, _, res = run_points(4, nl, pts)
-    dense_us = res[-1][0]
-    r = rowb(cfg)
-    F = cfg["d_ff"]
+    torch.cuda.synchronize()
+    taus = []
+    for w in ws:
+        sc = torch.cat([sffn.gate_scores(calib[i:i + 8], w, sffn.SCORE_GATE, workspace=sc_ws)
+                        for i in range(0, 256, 8)])
+        taus.append(torch.quantile(sc.flatten()[::4].float(),
+                                   torch.tensor([1.0 - a for a in c["sweep_a"]], device=dev)).tolist())
+    F, r = c["d_ff"], rowb(c)
+    dense_us = run_dense(ws, x, bufs, 1)
     sweep = []
-    for (a_t, (us, a)) in zip(cfg["sweep_a"], res[:-1]):
-        b = F * r * (1 + 2 * a)
-        sweep.append({"a_target": a_t, "a": round(a, 4), "us_per_token": round(us, 3),
-                      "gbps": round(b / (us * 1e-6) / 1e9, 1), "frac_hbm": round(b / (us * 1e-6) / 1e9 / hbm, 4),
-                      "speedup_vs_dense": round(dense_us / us, 3)})
-    # breakeven: the active fraction where the sparse call takes as long as the
-    # dense one (linear between the swept points; "<" / ">" outside the sweep)
+    for i, a_t in enumerate(c["sweep_a"]):
+        us = run_sparse(ws, x, bufs, 1, sffn.MODE_THRESHOLD, sffn.SCORE_GATE,
+                        [taus[l][i] if a_t < 1.0 else 0.0 for l in range(nl)])
+        a = float(bufs["n"].float().mean().item()) / F
+        sweep.append(point(us, F * r * (1 + 2 * a), a_target=a_t, a=round(a, 4),
+                           speedup_vs_dense=round(dense_us / us, 3)))
+    # breakeven: where the sparse call takes as long as the dense layer, linear
+    # between swept points ("<" / ">" outside the sweep)
     be = None
     for p0, p1 in zip(sweep, sweep[1:]):
         if p0["us_per_token"] <= dense_us <= p1["us_per_token"] and p1["us_per_token"] > p0["us_per_token"]:
-            be = round(p0["a"] + (dense_us - p0["us_per_token"]) * (p1["a"] - p0["a"]) / (
-                p1["us_per_token"] - p0["us_per_token"]), 3)
+            be = round(p0["a"] + (dense_us - p0["us_per_token"]) * (p1["a"] - p0["a"]) /
+                       (p1["us_per_token"] - p0["us_per_token"]), 3)
             break
     if be is None and sweep:
-        if sweep[0]["us_per_token"] > dense_us:
-            be = f"< {sweep[0]['a']}"
-        elif sweep[-1]["us_per_token"] < dense_us:
-            be = f"> {sweep[-1]['a']}"
-    out["int4_threshold_sweep"] = {"workload": "qwen2.5-3b-swiglu-int4g64: d_model 2048, d_ff 11008, 36 layers, "
-                                               "threshold on |SiLU(g)|*||W_down[:,j]||, B=1",
-                                   "dense_us_per_token": round(dense_us, 3),
-                                   "dense": "every neuron: threshold 0 on the gate-and-up score (gate and up rows "
-                                            "streamed together), every W_downT row",
-                                   "points": sweep, "breakeven_active_fraction": be}
+        be = f"< {sweep[0]['a']}" if sweep[0]["us_per_token"] > dense_us else (
+            f">= {sweep[-1]['a']}" if sweep[-1]["us_per_token"] <= dense_us else None)
+    out["int4_threshold_sweep"] = {
+        "workload": "qwen2.5-3b-swiglu-int4g64: d_model 2048, d_ff 11008, 36 layers, threshold on "
+                    "|SiLU(g)|*||W_down[:,j]||, B=1",
+        "dense": point(dense_us, 3 * F * r, kernel="sffn_decode_dense: every neuron, the three matrices read once"),
+        "points": sweep, "breakeven_active_fraction": be}
+    del layers, ws, x, bufs, sc_ws
     torch.cuda.empty_cache()
 
-    # keep-ratio tiers (gate-and-up score)
-    M = W.CONFIGS[3]["keep_M"]
-    cfg, _, _, _, res = run_points(3, W.CONFIGS[3]["layers"],
-                                   [(sffn.MODE_KEEP_RATIO, sffn.SCORE_GATE_UP, [1.0 / m] * 36) for m in M])
-    r = rowb(cfg)
-    F = cfg["d_ff"]
-    out["keep_ratio"] = {"workload": "qwen2.5-3b-swiglu: d_model 2048, d_ff 11008 bf16, 36 layers, "
-                                     "score |SiLU(g)*u|*||W_down[:,j]||, B=1",
-                         "by_M": {str(m): {"us_per_token": round(us, 3), "a": round(a, 4),
-                                           "gbps": round(F * r * (2 + a) / (us * 1e-6) / 1e9, 1)}
-                                  for m, (us, a) in zip(M, res)}}
-    torch.cuda.empty_cache()
-
-    # batched tokens on the Llama shape (union of active rows read once)
+    # ---- Llama shape, exact gating: batched tokens (the union of the tokens'
+    # active rows is read once) and the dense layer at B = 1
+    c = W.CONFIGS[2]
+    F, r = c["d_ff"], rowb(c)
     bt = {}
-    for B in (4, 8):
-        cfg, _, _, _, res = run_points(2, 8, [(sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0] * 8)], B=B)
-        bt[str(B)] = {"us_per_token": round(res[0][0], 3), "a_per_token": round(res[0][1], 4)}
+    for B in (1, 2, 4, 8):
+        layers, ws, x, bufs = setup(2, 8, B=B, norms=False)
+        us = run_sparse(ws, x, bufs, B, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0] * 8) / B
+        n = bufs["n"].cpu().numpy()
+        idx = bufs["idx"].cpu().numpy()
+        uni = np.mean([np.unique(np.concatenate([idx[t * B + b, : n[t * B + b]] for b in range(B)])).size
+                       for t in range(T)]) / F
+        bt[str(B)] = point(us, F * r * (1 + 2 * uni) / B, a_per_token=round(float(n.mean()) / F, 4),
+                           union_fraction=round(float(uni), 4))
+        if B == 1:
+            dus = run_dense(ws, x, bufs, 1)
+            bt["dense_B1"] = point(dus, 3 * F * r, speedup_of_sparse_B1=round(dus / us, 3))
+        del layers, ws, x, bufs
         torch.cuda.empty_cache()
-    out["batched_exact_llama"] = bt
+    out["llama_exact_by_batch"] = bt
 
-    # tiny fp32 ReGLU layer (L2 resident, launch bound: us/token only)
-    cfg, _, _, _, res = run_points(1, 1, [(sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0])])
-    out["tiny_fp32"] = {"us_per_token": round(res[0][0], 3), "a": round(res[0][1], 4)}
+    # ---- keep-ratio tiers: the gate-and-up score (W_up read in full, only W_down
+    # sparse) and the gate score (W_up and W_down sparse)
+    c = W.CONFIGS[3]
+    F, r = c["d_ff"], rowb(c)
+    layers, ws, x, bufs = setup(3, c["layers"])
+    kr = {}
+    for name, score in (("gate_up", sffn.SCORE_GATE_UP), ("gate", sffn.SCORE_GATE)):
+        by = {}
+        for M in c["keep_M"]:
+            us = run_sparse(ws, x, bufs, 1, sffn.MODE_KEEP_RATIO, score, [1.0 / M] * c["layers"])
+            a = float(bufs["n"].float().mean().item()) / F
+            by[str(M)] = point(us, F * r * ((2 + a) if score == sffn.SCORE_GATE_UP else (1 + 2 * a)), a=round(a, 4))
+        kr[name] = by
+    out["keep_ratio"] = {"workload": "qwen2.5-3b-swiglu: d_model 2048, d_ff 11008 bf16, 36 layers, keep the "
+                                     "top d_ff/M scores, B=1", "by_score": kr}
+    del layers, ws, x, bufs
+    torch.cuda.empty_cache()
+
+    # ---- tiny fp32 ReGLU layer (L2 resident, launch bound: us/token only)
+    layers, ws, x, bufs = setup(1, 1, norms=False)
+    us = run_sparse(ws, x, bufs, 1, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0])
+    out["tiny_fp32"] = {"us_per_token": round(us, 3), "a": round(float(bufs["n"].float().mean().item()) / 688, 4)}
     return out
 
 
@@ -496,6 +525,7 @@ def bench_prefill_stack(args, dev):
         out = torch.empty_like(X)
         sel = torch.empty((n, L), dtype=torch.int32, device=dev)
         ns = torch.empty(n, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()  # made on the default stream, used on `stream`
         res = {"workload": "4 token-selective prefill layers (L 16384, d_model 5120, d_ff 25600, SwiGLU bf16); "
                            "schedule: layer 0 dense, layers 1-2 mass 0.5, layer 3 mass 0.2, recent_n 128, "
                            "min_keep 1; synthetic attention outputs per layer"}
@@ -535,6 +565,7 @@ def bench_prefill(args, dev, rank, world, dist):
     n = torch.empty(1, dtype=torch.int32, device=dev)
     out = torch.empty_like(X)
     stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()  # made on the default stream, used on `stream`
     _, bf16_peak, _, peak_src = peaks()
     rows = {}
     for m in c["mass"]:
