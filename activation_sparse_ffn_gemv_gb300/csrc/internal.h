@@ -95,7 +95,7 @@ sffn_status run_down_norms(const sffn_ffn_weights *w, float *norms, cudaStream_t
 
 struct SelectPlan {
     int L, d;
-    size_t off_err, off_norms, off_flag, total;
+    size_t off_err, off_norms, off_flag, off_state, off_hist, off_cmax, total;
 };
 SelectPlan make_select_plan(int L, int d);
 sffn_status run_token_select(const void *y_attn, int L, int d, float mass_thresh, int recent_n, int min_keep,

@@ -112,6 +112,23 @@ def test_ties_take_lower_indices(sffn):
         assert sel.tolist() in (list(range(10)), list(range(11)))
 
 
+# 5000/7000 tokens stage in shared memory; 50000/70000 run the multi-block passes
+@pytest.mark.parametrize("k", [1, 10])
+def test_ties_across_many_blocks(sffn, k):
+    # 5000k equal importances of exactly 2 (every sum exact): a quarter of the
+    # mass is the first 1250k tokens, whichever blocks they fall in
+    row = torch.zeros(1, 64, dtype=torch.bfloat16)
+    row[0, 3] = 2.0
+    g, sel, _ = check_select(sffn, row.repeat(5000 * k, 1), 0.25, recent_n=0, min_keep=1)
+    assert g.tolist() == sel.tolist() == list(range(1250 * k))
+    # two values, the larger after the smaller: 4000k twos, then 3000k fours;
+    # 0.7 of the mass is every four and the first 1000k twos
+    ya = row.repeat(7000 * k, 1)
+    ya[4000 * k:, 3] = 4.0
+    g, sel, _ = check_select(sffn, ya, 0.7, recent_n=0, min_keep=1)
+    assert g.tolist() == sel.tolist() == list(range(1000 * k)) + list(range(4000 * k, 7000 * k))
+
+
 def test_recent_tail_longer_than_sequence(sffn):
     _, ya = W.make_prefill_inputs(50, 64, seed=3)
     g, _, _ = check_select(sffn, ya, 0.2, recent_n=128, min_keep=1)
