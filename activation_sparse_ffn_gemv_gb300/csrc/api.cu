@@ -4,6 +4,8 @@
 #include <mutex>
 
 #include "common.cuh"
+#include <cmath>
+
 #include "internal.h"
 
 namespace sffn {
@@ -226,6 +228,39 @@ sffn_status sffn_decode_dense(const void *x, int B, const sffn_ffn_weights *w, v
     c.out = out;
     c.ws = workspace;
     st = run_decode_tc(c, p, (cudaStream_t)stream, true);
+    if (st == SFFN_OK) st = cuda_status(cudaGetLastError());
+    return st;
+}
+
+sffn_status sffn_decode_predicted(const void *x, const sffn_ffn_weights *w, const float *factor_a,
+                                  const float *factor_b, int rank, float alpha, void *out, int32_t *active_idx,
+                                  int32_t *n_active, void *workspace, size_t ws_bytes, sffn_stream_t stream) {
+    sffn_status st = check_decode_args(x, 1, w, SFFN_MODE_EXACT, SFFN_SCORE_GATE, 0.f);
+    if (st != SFFN_OK) return st;
+    if (!out || !active_idx || !n_active) return SFFN_ERR_INVALID_ARG;
+    if (!aligned16(out)) return SFFN_ERR_ALIGNMENT;
+    if (w->wdtype != SFFN_BF16 && w->wdtype != SFFN_F32) return SFFN_ERR_UNSUPPORTED;
+    if (!(alpha >= 0.f)) return SFFN_ERR_INVALID_ARG;  // also rejects NaN
+    if (!std::isinf(alpha)) {
+        if (!factor_a || !factor_b) return SFFN_ERR_INVALID_ARG;
+        if (rank < 1 || rank > w->d_ff || rank > 4096) return SFFN_ERR_SHAPE;
+        if (!aligned16(factor_b)) return SFFN_ERR_ALIGNMENT;
+    }
+    if (device_sm_count() <= 0) return SFFN_ERR_CUDA;
+    DecodePlan p = make_decode_plan(1, w->d_model, w->d_ff);
+    st = check_ws(workspace, ws_bytes, p.total);
+    if (st != SFFN_OK) return st;
+    DecodeCall c = {};
+    c.x = x;
+    c.w = w;
+    c.B = 1;
+    c.mode = SFFN_MODE_EXACT;
+    c.score = SFFN_SCORE_GATE;
+    c.out = out;
+    c.active_idx = active_idx;
+    c.n_active = n_active;
+    c.ws = workspace;
+    st = run_decode_predicted(c, p, factor_a, factor_b, rank, alpha, (cudaStream_t)stream);
     if (st == SFFN_OK) st = cuda_status(cudaGetLastError());
     return st;
 }

@@ -20,129 +20,9 @@
 #include "common.cuh"
 #include "decode_finish.cuh"
 #include "internal.h"
+#include "wformat.cuh"
 
 namespace sffn {
-
-// ---------------------------------------------------------------------------
-// weight formats: a 16-byte unit of a stored row
-// ---------------------------------------------------------------------------
-
-struct WF32 {
-    using X = float;                 // activation dtype that goes with these weights
-    static constexpr int E = 4;      // elements per 16-byte unit
-    static SFFN_DEV void unpack(const uint4 &v, float *f) {
-        f[0] = __uint_as_float(v.x);
-        f[1] = __uint_as_float(v.y);
-        f[2] = __uint_as_float(v.z);
-        f[3] = __uint_as_float(v.w);
-    }
-    static constexpr bool Q = false;  // no group scales
-    static SFFN_DEV float scale_at(const unsigned char *, uint32_t) { return 1.f; }
-    static SFFN_DEV void dequant(const uint4 &v, float, float *f) { unpack(v, f); }
-    // x elements matching weight unit u (x stored in its own dtype, 16-byte units)
-    static SFFN_DEV void load_xu(const uint4 *xrow, uint32_t u, float *f) { unpack(xrow[u], f); }
-};
-
-struct WBF16 {
-    using X = __nv_bfloat16;
-    static constexpr int E = 8;
-    static SFFN_DEV void unpack(const uint4 &v, float *f) {
-        f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
-        f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
-        f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
-        f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
-    }
-    static constexpr bool Q = false;
-    static SFFN_DEV float scale_at(const unsigned char *, uint32_t) { return 1.f; }
-    static SFFN_DEV void dequant(const uint4 &v, float, float *f) { unpack(v, f); }
-    static SFFN_DEV void load_xu(const uint4 *xrow, uint32_t u, float *f) { unpack(xrow[u], f); }
-};
-
-// Symmetric int4 with one fp16 scale per 64 consecutive elements of a stored
-// row: a 16-byte unit holds 32 two's-complement codes (low nibble = even
-// column) and lies in group u / 2.  code * scale is exact in fp32, and so is its
-// product with a bf16 activation (at most 23 significant bits).
-struct WINT4 {
-    using X = __nv_bfloat16;
-    static constexpr int E = 32;
-    static constexpr bool Q = true;
-    static SFFN_DEV float scale_at(const unsigned char *srow, uint32_t u) {
-        return __half2float(*reinterpret_cast<const __half *>(srow + (u >> 1) * 2));
-    }
-    // nibble n (two's complement) -> n ^ 8 is the code + 8 as an unsigned value;
-    // OR-ing it into the mantissa of 2^23 gives 2^23 + code + 8 exactly
-    static SFFN_DEV void codes(const uint4 &v, float *f) {
-        const uint32_t w[4] = {v.x ^ 0x88888888u, v.y ^ 0x88888888u, v.z ^ 0x88888888u, v.w ^ 0x88888888u};
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                f[8 * q + k] = __uint_as_float(0x4B000000u | ((w[q] >> (4 * k)) & 0xFu)) - 8388616.0f;
-    }
-    static SFFN_DEV void dequant(const uint4 &v, float s, float *f) {
-        codes(v, f);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) f[e] *= s;
-    }
-    static SFFN_DEV void load_xu(const uint4 *xrow, uint32_t u, float *f) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) WBF16::unpack(xrow[4 * u + q], f + 8 * q);
-    }
-};
-
-// Copy the activations x [nb, d] into shared memory in their own dtype
-// [NBpad, d] (rows >= nb zero), 128-bit units, four loads in flight per thread.
-template <class W>
-SFFN_DEV void stage_x_raw(void *xs, const void *x, int nb, int NBpad, int d) {
-    constexpr int XE = 16 / (int)sizeof(typename W::X);
-    const int per_row = d / XE;
-    const int total = NBpad * per_row;
-    uint4 *dst = static_cast<uint4 *>(xs);
-    for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
-        uint4 v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int u = base + k * blockDim.x;
-            v[k] = (u < total && u / per_row < nb) ? ldg_v4(static_cast<const char *>(x) + (size_t)u * 16)
-                                                   : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int u = base + k * blockDim.x;
-            if (u < total) dst[u] = v[k];
-        }
-    }
-}
-
-// Stage the activations x [nb, d] into shared memory as fp32 [NBpad, d]
-// (rows >= nb zero).  128-bit loads, four in flight per thread, so staging
-// costs one memory round trip instead of one per element.
-template <class W>
-SFFN_DEV void stage_x(float *xs, const void *x, int nb, int NBpad, int d) {
-    constexpr int XE = 16 / (int)sizeof(typename W::X);  // elements per 16-byte unit of x
-    const int per_row = d / XE;
-    const int total = NBpad * per_row;
-    for (int base = threadIdx.x; base < total; base += 4 * blockDim.x) {
-        uint4 v[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int u = base + k * blockDim.x;
-            v[k] = (u < total && u / per_row < nb) ? ldg_v4(static_cast<const char *>(x) + (size_t)u * 16)
-                                                   : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const int u = base + k * blockDim.x;
-            if (u < total) {
-                float f[XE];
-                W::unpack(v[k], f);
-                float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)u * XE);
-#pragma unroll
-                for (int q = 0; q < XE / 4; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);
-            }
-        }
-    }
-}
 
 // ---------------------------------------------------------------------------
 // down-projection column norms: norms[j] = ||W_downT[j, :]||_2
@@ -679,15 +559,41 @@ SFFN_DEV int find_cross_bin(const unsigned *hist, int nbins, unsigned need, unsi
     return bin;
 }
 
+// Scores of one token are staged in shared memory up to this many neurons.
+constexpr int kKeepStage = 40960;
+
+// One CTA per token.  The token's scores are staged in shared memory (when F
+// fits) for the three digit passes (count histograms: 32-bit shared atomic
+// increments).  The ordered compaction gives each warp a contiguous chunk of
+// whole 32-neuron mask words: a ballot over 32 consecutive neurons is the
+// token's mask word, and ballot popcounts rank the selected neurons
+// (ascending) without atomics.
 __global__ void __launch_bounds__(kSelThreads) k_keep_ratio(KeepArgs a) {
+    extern __shared__ __align__(16) uint32_t skey[];  // [F] staged score bits (F <= kKeepStage)
     __shared__ unsigned hist[2048];
     __shared__ int tmp[34];
-    __shared__ uint32_t smask[2048];  // F <= 65536
     griddep_wait();
     griddep_launch_dependents();
-    const int b = blockIdx.x, tid = threadIdx.x;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int F = a.F;
     const uint32_t *key = reinterpret_cast<const uint32_t *>(a.score + (size_t)b * F);
+    if (F <= kKeepStage) {
+        for (int j0 = tid; j0 < F; j0 += 8 * blockDim.x) {
+            uint32_t v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int j = j0 + k * blockDim.x;
+                v[k] = j < F ? key[j] : 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int j = j0 + k * blockDim.x;
+                if (j < F) skey[j] = v[k];
+            }
+        }
+        key = skey;
+        __syncthreads();
+    }
 
     // three digit passes: bits 31..21, 20..10, 9..0
     uint32_t prefix = 0, pmask = 0;
@@ -712,42 +618,59 @@ __global__ void __launch_bounds__(kSelThreads) k_keep_ratio(KeepArgs a) {
     const uint32_t T = prefix;        // bits of the k-th largest score
     const unsigned take_eq = need;    // how many scores equal to T are kept (lowest index first)
 
-    // ordered compaction over contiguous segments
-    const int seg = (F + blockDim.x - 1) / blockDim.x;
-    const int j0 = min(F, tid * seg), j1 = min(F, j0 + seg);
-    int eq = 0;
-    for (int j = j0; j < j1; ++j) eq += key[j] == T;
-    int tot;
-    const int eq_base = block_excl_scan(eq, tmp, &tot);
-    int nsel = 0, eq_seen = 0;
-    for (int j = j0; j < j1; ++j) {
-        const uint32_t kv = key[j];
-        const bool s = kv > T || (kv == T && (unsigned)(eq_base + eq_seen) < take_eq);
-        eq_seen += kv == T;
-        nsel += s;
+    // ordered compaction: warp chunks of whole mask words
+    const int nwords = (F + 31) >> 5, nw = blockDim.x >> 5;
+    const int wchunk = (nwords + nw - 1) / nw;
+    const int w0 = min(nwords, warp * wchunk), w1 = min(nwords, w0 + wchunk);
+    int gt = 0, eq = 0;
+    for (int w = w0; w < w1; ++w) {
+        const int j = 32 * w + lane;
+        const uint32_t kv = j < F ? key[j] : 0u;
+        gt += __popc(__ballot_sync(0xffffffffu, j < F && kv > T));
+        eq += __popc(__ballot_sync(0xffffffffu, j < F && kv == T));
     }
-    const int sel_base = block_excl_scan(nsel, tmp, &tot);
-    const int nw = (F + 31) >> 5;
-    for (int i = tid; i < nw; i += blockDim.x) smask[i] = 0;
-    __syncthreads();
-    int pos = sel_base;
-    eq_seen = 0;
-    for (int j = j0; j < j1; ++j) {
-        const uint32_t kv = key[j];
-        const bool s = kv > T || (kv == T && (unsigned)(eq_base + eq_seen) < take_eq);
-        eq_seen += kv == T;
-        if (s) {
-            if (a.lh && a.nb == 1) a.lh[pos] = a.aeff[j] * a.uval[j];
-            a.lidx[(size_t)b * F + pos++] = j;
-            atomicOr(&smask[j >> 5], 1u << (j & 31));
-        } else {
-            a.aeff[(size_t)b * F + j] = 0.f;
+    int tot;
+    const int eq_base = __shfl_sync(0xffffffffu, block_excl_scan(lane == 0 ? eq : 0, tmp, &tot), 0);
+    const int eq_take = (int)min((unsigned)eq, take_eq > (unsigned)eq_base ? take_eq - (unsigned)eq_base : 0u);
+    int pos = __shfl_sync(0xffffffffu, block_excl_scan(lane == 0 ? gt + eq_take : 0, tmp, &tot), 0);
+    int eq_seen = eq_base;
+    const unsigned lt = (1u << lane) - 1u;
+    const bool want_h = a.lh && a.nb == 1;  // h_j = a_j * u_j for the selected neurons
+    float *aeff = a.aeff + (size_t)b * F;
+    int32_t *lidx = a.lidx + (size_t)b * F;
+    constexpr int U = 4;  // mask words per step: the a_j, u_j loads of a step are issued together
+    for (int w = w0; w < w1; w += U) {
+        float av[U], uv[U];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            const int j = 32 * (w + q) + lane;
+            const bool ld = want_h && w + q < w1 && j < F;
+            av[q] = ld ? aeff[j] : 0.f;
+            uv[q] = ld ? a.uval[j] : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            if (w + q >= w1) break;
+            const int j = 32 * (w + q) + lane;
+            const bool ok = j < F;
+            const uint32_t kv = ok ? key[j] : 0u;
+            const bool e = ok && kv == T;
+            const unsigned ebal = __ballot_sync(0xffffffffu, e);
+            const bool sel = ok && (kv > T || (e && (unsigned)(eq_seen + __popc(ebal & lt)) < take_eq));
+            const unsigned sbal = __ballot_sync(0xffffffffu, sel);
+            if (sel) {
+                const int r = pos + __popc(sbal & lt);
+                if (want_h) a.lh[r] = av[q] * uv[q];
+                lidx[r] = j;
+            } else if (ok) {
+                aeff[j] = 0.f;
+            }
+            if (lane == 0 && a.mask) a.mask[(size_t)b * nwords + w + q] = sbal;
+            pos += __popc(sbal);
+            eq_seen += __popc(ebal);
         }
     }
-    __syncthreads();
     for (int c = tid; c < a.C; c += blockDim.x) a.cnt[(size_t)b * a.C + c] = c == 0 ? tot : 0;
-    if (a.mask)
-        for (int i = tid; i < nw; i += blockDim.x) a.mask[(size_t)b * nw + i] = smask[i];
 }
 
 // union of the per-token keep-ratio selections (nb > 1), ascending
@@ -1341,7 +1264,11 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
             ka.cnt = cnt;
             ka.lidx = lidx;
             ka.mask = p.nb > 1 ? mask : nullptr;
-            e = launch_k(k_keep_ratio, dim3(p.nb), dim3(kSelThreads), 0, s, ka);
+            const size_t ksm = p.F <= kKeepStage ? sizeof(uint32_t) * (size_t)p.F : 0;
+            if (ksm && (e = set_max_smem((const void *)k_keep_ratio, (int)(sizeof(uint32_t) * kKeepStage))) !=
+                           cudaSuccess)
+                return e;
+            e = launch_k(k_keep_ratio, dim3(p.nb), dim3(kSelThreads), ksm, s, ka);
             if (e != cudaSuccess) return e;
             if (p.nb > 1) {
                 e = launch_k(k_union, dim3(1), dim3(kSelThreads), 0, s, (const uint32_t *)mask, p.nb, p.F, p.C, cnt, lidx,
@@ -1427,6 +1354,32 @@ static cudaError_t launch_decode_w(const DecodeCall &c, const DecodePlan &p, cud
     if (p.nb == 2) return launch_decode_t<W, 2>(c, p, s);
     if (p.nb <= 4) return launch_decode_t<W, 4>(c, p, s);
     return launch_decode_t<W, 8>(c, p, s);
+}
+
+// The finish of a one-token decode whose C gate chunks have each written a
+// partial output part[c, d] and an ascending list of its active neurons
+// (cnt [C], lidx [C, R]): the fixed-order sum of the partials into `out`, and
+// the token's list and count.
+sffn_status run_reduce_chunks(const DecodeCall &c, const DecodePlan &p, cudaStream_t s) {
+    char *ws = static_cast<char *>(c.ws);
+    ReduceArgs ra = {};
+    ra.part = reinterpret_cast<float *>(ws + p.off_part);
+    ra.G2 = p.C;
+    ra.nb = 1;
+    ra.d = p.d;
+    ra.out = c.out;
+    ra.out_f32 = c.w->wdtype == SFFN_F32;
+    ra.n_red = (p.d + 31) / 32;
+    ra.C = p.C;
+    ra.R = p.R;
+    ra.F = p.F;
+    ra.cnt = reinterpret_cast<int *>(ws + p.off_cnt);
+    ra.lidx = reinterpret_cast<int *>(ws + p.off_lidx);
+    ra.active_idx = c.active_idx;
+    ra.n_active = c.n_active;
+    const int list_grid = (p.C + kListChunks - 1) / kListChunks;
+    const cudaError_t e = launch_k(k_reduce, dim3(ra.n_red + list_grid), dim3(256), 0, s, ra);
+    return e == cudaSuccess ? SFFN_OK : SFFN_ERR_CUDA;
 }
 
 sffn_status run_decode(const DecodeCall &c, const DecodePlan &p, cudaStream_t s) {

@@ -88,6 +88,12 @@ bool decode_tc_shape_ok(const sffn_ffn_weights *w, const DecodePlan &p);
 bool decode_tc_eligible(const DecodeCall &c, const DecodePlan &p);
 sffn_status run_decode_tc(const DecodeCall &c, const DecodePlan &p, cudaStream_t s, bool dense);
 sffn_status run_down_norms(const sffn_ffn_weights *w, float *norms, cudaStream_t s);
+// One-token finish over per-chunk partials and lists in the workspace (part
+// [C, d], cnt [C], lidx [C, R]): the fixed-order reduction and the list writes.
+sffn_status run_reduce_chunks(const DecodeCall &c, const DecodePlan &p, cudaStream_t s);
+// Decode with the low-rank gate predictor (predict.cu): one token, bf16 / fp32.
+sffn_status run_decode_predicted(const DecodeCall &c, const DecodePlan &p, const float *factor_a,
+                                 const float *factor_b, int rank, float alpha, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Token selection / prefill

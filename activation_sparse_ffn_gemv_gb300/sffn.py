@@ -73,6 +73,8 @@ def lib():
         L.sffn_decode.restype = I
         L.sffn_decode_dense.argtypes = [P, I, W, P, P, S, P]
         L.sffn_decode_dense.restype = I
+        L.sffn_decode_predicted.argtypes = [P, W, P, P, I, F, P, P, P, P, S, P]
+        L.sffn_decode_predicted.restype = I
         L.sffn_gate_scores.argtypes = [P, I, W, I, P, P, S, P]
         L.sffn_gate_scores.restype = I
         L.sffn_token_select.argtypes = [P, I, I, F, I, I, P, P, P, S, P]
@@ -192,6 +194,28 @@ def decode_dense(x: torch.Tensor, w: Weights, out=None, workspace=None, stream=N
     st = lib().sffn_decode_dense(_ptr(x), B, w.ref(), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "sffn_decode_dense")
     return out
+
+
+def decode_predicted(x: torch.Tensor, w: Weights, factor_a, factor_b, alpha: float, out=None, active_idx=None,
+                     n_active=None, workspace=None, stream=None):
+    """One token with the low-rank gate predictor: factor_a [d_ff, r] and
+    factor_b [r, d] fp32 on the device (None with alpha = inf).  Returns
+    (out [1, d], active_idx [1, d_ff], n_active [1])."""
+    if out is None:
+        out = torch.empty_like(x)
+    if active_idx is None:
+        active_idx = torch.empty((1, w.d_ff), dtype=torch.int32, device=x.device)
+    if n_active is None:
+        n_active = torch.empty(1, dtype=torch.int32, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(WS_DECODE, 1, w, x.device)
+    rank = 0 if factor_a is None else int(factor_a.shape[1])
+    pa = None if factor_a is None else _ptr(factor_a)
+    pb = None if factor_b is None else _ptr(factor_b)
+    st = lib().sffn_decode_predicted(_ptr(x), w.ref(), pa, pb, rank, float(alpha), _ptr(out), _ptr(active_idx),
+                                     _ptr(n_active), _ptr(workspace), workspace.numel(), _stream(stream))
+    _check(st, "sffn_decode_predicted")
+    return out, active_idx, n_active
 
 
 def decode_noalloc(x: torch.Tensor, w: Weights, mode: int, score: int = SCORE_GATE, param: float = 0.0,

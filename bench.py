@@ -477,6 +477,51 @@ def bench_decode_sweeps(args, dev, T=256):
     del layers, ws, x, bufs
     torch.cuda.empty_cache()
 
+    # ---- low-rank gate predictor on the Llama shape (sffn_decode_predicted):
+    # random rank-256 fp32 factors (timing only: quality needs trained weights),
+    # A scaled so that A (B x) spreads like the gate bias; alpha per layer so a
+    # target share of the timed tokens' neurons are candidates
+    c = W.CONFIGS[2]
+    F, d, nl, rank = c["d_ff"], c["d_model"], c["layers"], 256
+    layers, ws, x, bufs = setup(2, nl, norms=False)
+    gen = torch.Generator(device=dev).manual_seed(11)
+    xt = x[:T].float()
+    facs, preds = [], []
+    for l in range(nl):
+        A = torch.randn(F, rank, generator=gen, device=dev) / rank ** 0.5
+        Bf = torch.randn(rank, d, generator=gen, device=dev) / d ** 0.5
+        q = (xt @ Bf.t()) @ A.t()
+        A = (A * (0.5 / q.std())).contiguous()
+        bias = layers[l]["b_gate"].to(dev).float()
+        facs.append((A, Bf.contiguous()))
+        preds.append((xt @ Bf.t()) @ A.t() + bias[None, :])
+    exact_us = run_sparse(ws, x, bufs, 1, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0] * nl)
+    lr = {"workload": "llama2-7b-reglu shape (d_model 4096, d_ff 11008 bf16, 8 layers), B=1, rank-256 fp32 "
+                      "factors (random: timing only), exact rule on the candidates",
+          "exact_decode_us_per_token": round(exact_us, 3), "points": []}
+    for frac in (0.15, 0.3, 0.5):
+        alphas, cand = [], []
+        for l in range(nl):
+            v = torch.quantile(preds[l][l::nl].flatten(), 1.0 - frac).item()
+            alphas.append(max(0.0, -v))
+            cand.append((preds[l][l::nl] >= -alphas[-1]).float().mean().item())
+
+        def enq():
+            for t in range(T):
+                A, Bf = facs[t % nl]
+                sffn.decode_predicted(x[t:t + 1], ws[t % nl], A, Bf, alphas[t % nl], out=bufs["o"][t:t + 1],
+                                      active_idx=bufs["idx"][t:t + 1], n_active=bufs["n"][t:t + 1],
+                                      workspace=bufs["work"], stream=stream)
+        us = _time_graph(enq, stream, max(3, args.steps // 3), args.warmup) * 1e3 / T
+        a = float(bufs["n"][:T].float().mean().item()) / F
+        cf = sum(cand) / nl
+        nbytes = 4.0 * rank * (F + d) + rowb(c) * F * (cf + 2 * a)
+        lr["points"].append(point(us, nbytes, candidates=round(cf, 4), a=round(a, 4),
+                                  speedup_vs_exact=round(exact_us / us, 3)))
+    out["lowrank_predictor"] = lr
+    del layers, ws, x, bufs, facs, preds
+    torch.cuda.empty_cache()
+
     # ---- tiny fp32 ReGLU layer (L2 resident, launch bound: us/token only)
     layers, ws, x, bufs = setup(1, 1, norms=False)
     us = run_sparse(ws, x, bufs, 1, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0])

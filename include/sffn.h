@@ -147,6 +147,31 @@ sffn_status sffn_decode(const void *x, int B, const sffn_ffn_weights *w, int mod
 sffn_status sffn_decode_dense(const void *x, int B, const sffn_ffn_weights *w, void *out, void *workspace,
                               size_t ws_bytes, sffn_stream_t stream);
 
+/* Decode one token through one layer with the low-rank gate predictor of the
+ * denseflux write-up ("skipping most of a dense FFN", sec. 4.3, cheap
+ * predictors: the best untrained predictor is low-rank).  The factors
+ * W_gate ~= A B are made offline (e.g. a rank-r truncated SVD of the dequantised
+ * gate); per token
+ *   y = B x,  p_j = A[j, :] . y + b_gate[j],  candidates P = { j : p_j >= -alpha },
+ * the exact gate g_j = W_gate[j, :] . x + b_gate[j] only for j in P, and
+ * j active iff j in P and act(g_j) != 0 (the exact rule).  A neuron outside P
+ * is skipped even when it would have been active.
+ *   x          [d_model], bf16 (fp32 with fp32 weights); 16-byte aligned.
+ *   w          bf16 or fp32 weights (int4-g64: SFFN_ERR_UNSUPPORTED).
+ *   factor_a   A [d_ff, rank] fp32 row-major, device memory.
+ *   factor_b   B [rank, d_model] fp32 row-major, device memory, 16-byte aligned.
+ *   rank       1 <= rank <= min(d_ff, 4096).
+ *   alpha      >= 0; +INFINITY makes every neuron a candidate (the factors are
+ *              then not read and may be NULL): the exact decode.
+ *   out, active_idx [d_ff], n_active [1]: as sffn_decode with B = 1 (active
+ *              neurons ascending).
+ *   workspace  sffn_workspace_size(0, 1, w) bytes, 16-byte aligned.
+ * The caller owns every buffer; nothing is allocated.  Argument errors are
+ * returned before anything is enqueued. */
+sffn_status sffn_decode_predicted(const void *x, const sffn_ffn_weights *w, const float *factor_a,
+                                  const float *factor_b, int rank, float alpha, void *out, int32_t *active_idx,
+                                  int32_t *n_active, void *workspace, size_t ws_bytes, sffn_stream_t stream);
+
 /* Size of the scratch array built into the library for sffn_decode_noalloc. */
 #define SFFN_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -144,6 +144,39 @@ def test_dense_layer_argument_checks(S):
     assert L.sffn_decode_dense(16, 1, None, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
 
 
+def test_predicted_decode_argument_checks(S):
+    # every check before the device is touched (on a machine without a GPU a
+    # call that passes them all stops at the device check: ERR_CUDA)
+    L = S.lib()
+    inf = float("inf")
+
+    def wts(**kw):
+        f = dict(wdtype=S.BF16, act=S.ACT_RELU, d_model=64, d_ff=128)
+        f.update(kw)
+        return S.FFNWeights(f["wdtype"], f["act"], f["d_model"], f["d_ff"], 16, 16, 16, 16, 16, 16, None, None)
+
+    def pred(w, x=16, fa=16, fb=16, rank=8, alpha=0.5, out=16, idx=16, n=16):
+        return L.sffn_decode_predicted(x, C.byref(w), fa, fb, rank, alpha, out, idx, n, 256, 1 << 20, None)
+
+    assert pred(wts(), x=None) == S.ERR_INVALID_ARG
+    assert pred(wts(), out=None) == S.ERR_INVALID_ARG
+    assert pred(wts(), idx=None) == S.ERR_INVALID_ARG
+    assert pred(wts(), n=None) == S.ERR_INVALID_ARG
+    assert pred(wts(), out=8) == S.ERR_ALIGNMENT
+    assert pred(wts(wdtype=S.INT4_G64, d_model=512)) == S.ERR_UNSUPPORTED
+    assert pred(wts(), alpha=-0.5) == S.ERR_INVALID_ARG
+    assert pred(wts(), alpha=float("nan")) == S.ERR_INVALID_ARG
+    assert pred(wts(), fa=None) == S.ERR_INVALID_ARG
+    assert pred(wts(), fb=None) == S.ERR_INVALID_ARG
+    assert pred(wts(), rank=0) == S.ERR_SHAPE
+    assert pred(wts(), rank=129) == S.ERR_SHAPE          # rank <= d_ff
+    assert pred(wts(), fb=24) == S.ERR_ALIGNMENT
+    assert pred(wts(d_model=8192)) == S.ERR_SHAPE
+    assert L.sffn_decode_predicted(16, None, 16, 16, 8, 0.5, 16, 16, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+    # alpha = +inf: the factors are not read and may be null
+    assert pred(wts(), fa=None, fb=None, rank=0, alpha=inf) not in (S.ERR_INVALID_ARG, S.ERR_SHAPE)
+
+
 @pytest.mark.gpu
 def test_workspace_checks_on_gpu(S):
     from activation_sparse_ffn_gemv_gb300 import workloads as W
