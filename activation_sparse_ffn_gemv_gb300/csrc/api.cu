@@ -265,6 +265,52 @@ sffn_status sffn_decode_predicted(const void *x, const sffn_ffn_weights *w, cons
     return st;
 }
 
+sffn_status sffn_decode_tiered(const void *x, int B, const sffn_ffn_weights *w, int score, float keep_ratio,
+                               const int32_t *core_idx, int n_core, void *out, int32_t *active_idx, int32_t *n_active,
+                               void *workspace, size_t ws_bytes, sffn_stream_t stream) {
+    sffn_status st = validate_decode_call(x, B, w, SFFN_MODE_KEEP_RATIO, score, keep_ratio, out, active_idx, n_active);
+    if (st != SFFN_OK) return st;
+    if (n_core < 0 || n_core > w->d_ff) return SFFN_ERR_SHAPE;
+    if (n_core > 0 && !core_idx) return SFFN_ERR_INVALID_ARG;
+    DecodePlan p = make_decode_plan(B, w->d_model, w->d_ff);
+    st = check_ws(workspace, ws_bytes, p.total);
+    if (st != SFFN_OK) return st;
+    DecodeCall c = {};
+    c.x = x;
+    c.w = w;
+    c.B = B;
+    c.mode = SFFN_MODE_KEEP_RATIO;
+    c.score = score;
+    c.param = keep_ratio;
+    c.out = out;
+    c.active_idx = active_idx;
+    c.n_active = n_active;
+    c.ws = workspace;
+    c.core = n_core > 0 ? core_idx : nullptr;
+    c.n_core = n_core;
+    st = run_decode(c, p, (cudaStream_t)stream);
+    if (st == SFFN_OK) st = cuda_status(cudaGetLastError());
+    return st;
+}
+
+size_t sffn_tier_core_workspace_size(int n_calib, int d_ff) {
+    if (n_calib < 1 || n_calib > (1 << 16) || d_ff < 1 || d_ff > 65536) return 0;
+    return tier_core_workspace(n_calib, d_ff);
+}
+
+sffn_status sffn_tier_core_set(const float *calib_scores, int n_calib, int d_ff, int k, int n_core, int32_t *core_idx,
+                               void *workspace, size_t ws_bytes, sffn_stream_t stream) {
+    if (!calib_scores || (n_core > 0 && !core_idx)) return SFFN_ERR_INVALID_ARG;
+    if (n_calib < 1 || n_calib > (1 << 16) || d_ff < 1 || d_ff > 65536) return SFFN_ERR_SHAPE;
+    if (k < 1 || k > d_ff || n_core < 0 || n_core > d_ff) return SFFN_ERR_INVALID_ARG;
+    if (device_sm_count() <= 0) return SFFN_ERR_CUDA;
+    sffn_status st = check_ws(workspace, ws_bytes, tier_core_workspace(n_calib, d_ff));
+    if (st != SFFN_OK) return st;
+    st = run_tier_core_set(calib_scores, n_calib, d_ff, k, n_core, core_idx, workspace, (cudaStream_t)stream);
+    if (st == SFFN_OK) st = cuda_status(cudaGetLastError());
+    return st;
+}
+
 sffn_status sffn_gate_scores(const void *x, int B, const sffn_ffn_weights *w, int score, float *scores,
                              void *workspace, size_t ws_bytes, sffn_stream_t stream) {
     sffn_status st = check_decode_args(x, B, w, SFFN_MODE_THRESHOLD, score, 0.f);

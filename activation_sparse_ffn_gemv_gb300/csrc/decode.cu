@@ -20,6 +20,7 @@
 #include "common.cuh"
 #include "decode_finish.cuh"
 #include "internal.h"
+#include "topk.cuh"
 #include "wformat.cuh"
 
 namespace sffn {
@@ -537,140 +538,82 @@ struct KeepArgs {
     int F, k, nb, C;
     int *cnt, *lidx;
     uint32_t *mask;      // [nb, ceil(F/32)] selection bitmask (nb > 1)
+    const int32_t *core; // the layer's core set (always kept; the top-k runs on the rest), or null
+    int n_core;
+    int32_t *err;        // the workspace's error word (a core index out of range)
 };
-
-// Find, over 2^bits bins scanned from the top, the bin where the running count
-// reaches `need`.  Returns the bin; *above = count in higher bins.
-SFFN_DEV int find_cross_bin(const unsigned *hist, int nbins, unsigned need, unsigned *above, int *tmp) {
-    // each thread owns up to 2 consecutive bins in descending order
-    const int t = threadIdx.x;
-    const int b0 = nbins - 1 - 2 * t, b1 = b0 - 1;
-    const unsigned c0 = b0 >= 0 ? hist[b0] : 0u, c1 = b1 >= 0 ? hist[b1] : 0u;
-    int total;
-    const unsigned ex = (unsigned)block_excl_scan((int)(c0 + c1), tmp, &total);
-    __shared__ int s_bin;
-    __shared__ unsigned s_above;
-    if (b0 >= 0 && ex < need && ex + c0 >= need) { s_bin = b0; s_above = ex; }
-    if (b1 >= 0 && ex + c0 < need && ex + c0 + c1 >= need) { s_bin = b1; s_above = ex + c0; }
-    __syncthreads();
-    const int bin = s_bin;
-    *above = s_above;
-    __syncthreads();
-    return bin;
-}
 
 // Scores of one token are staged in shared memory up to this many neurons.
 constexpr int kKeepStage = 40960;
 
 // One CTA per token.  The token's scores are staged in shared memory (when F
-// fits) for the three digit passes (count histograms: 32-bit shared atomic
-// increments).  The ordered compaction gives each warp a contiguous chunk of
-// whole 32-neuron mask words: a ballot over 32 consecutive neurons is the
-// token's mask word, and ballot popcounts rank the selected neurons
-// (ascending) without atomics.
+// fits) for the top-k (topk.cuh).  With a core set the core columns are always
+// kept and the select takes the k - |core| largest scores of the other columns
+// (none when the core holds k or more).  The ordered pass writes the token's
+// ascending list, its mask words, and zeroes a_j outside the selection.
 __global__ void __launch_bounds__(kSelThreads) k_keep_ratio(KeepArgs a) {
     extern __shared__ __align__(16) uint32_t skey[];  // [F] staged score bits (F <= kKeepStage)
     __shared__ unsigned hist[2048];
     __shared__ int tmp[34];
+    __shared__ uint32_t fmask[2048];  // the core as a bitmask (F <= 65536)
     griddep_wait();
     griddep_launch_dependents();
-    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int F = a.F;
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    const int F = a.F, nwords = (F + 31) >> 5;
     const uint32_t *key = reinterpret_cast<const uint32_t *>(a.score + (size_t)b * F);
     if (F <= kKeepStage) {
-        for (int j0 = tid; j0 < F; j0 += 8 * blockDim.x) {
-            uint32_t v[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int j = j0 + k * blockDim.x;
-                v[k] = j < F ? key[j] : 0u;
-            }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int j = j0 + k * blockDim.x;
-                if (j < F) skey[j] = v[k];
-            }
-        }
+        stage_keys(skey, key, F);
         key = skey;
-        __syncthreads();
     }
-
-    // three digit passes: bits 31..21, 20..10, 9..0
-    uint32_t prefix = 0, pmask = 0;
-    unsigned need = (unsigned)a.k;
-    const int shifts[3] = {21, 10, 0};
-    const int widths[3] = {11, 11, 10};
-    for (int pass = 0; pass < 3; ++pass) {
-        const int sh = shifts[pass], nbins = 1 << widths[pass];
-        for (int i = tid; i < nbins; i += blockDim.x) hist[i] = 0;
+    const uint32_t *forced = nullptr;
+    unsigned kk = (unsigned)a.k;
+    if (a.core) {
+        for (int i = tid; i < nwords; i += blockDim.x) fmask[i] = 0u;
         __syncthreads();
-        for (int j = tid; j < F; j += blockDim.x) {
-            const uint32_t kv = key[j];
-            if ((kv & pmask) == prefix) atomicAdd(&hist[(kv >> sh) & (nbins - 1)], 1u);
+        for (int q = tid; q < a.n_core; q += blockDim.x) {
+            const int j = a.core[q];
+            if (j >= 0 && j < F) atomicOr(&fmask[j >> 5], 1u << (j & 31));
+            else if (b == 0) record_error(a.err, SFFN_ERR_DEVICE);
         }
         __syncthreads();
-        unsigned above;
-        const int bin = find_cross_bin(hist, nbins, need, &above, tmp);
-        prefix |= (uint32_t)bin << sh;
-        pmask |= (uint32_t)(nbins - 1) << sh;
-        need -= above;
+        int c = 0;
+        for (int i = tid; i < nwords; i += blockDim.x) c += __popc(fmask[i]);
+        int c_eff;
+        block_excl_scan(c, tmp, &c_eff);
+        kk = kk > (unsigned)c_eff ? kk - (unsigned)c_eff : 0u;
+        forced = fmask;
     }
-    const uint32_t T = prefix;        // bits of the k-th largest score
-    const unsigned take_eq = need;    // how many scores equal to T are kept (lowest index first)
+    const TopkCut cut = radix_topk(key, F, kk, forced, hist, tmp);
+    TopkChunk ch = topk_chunk(key, F, forced, cut, tmp);
 
-    // ordered compaction: warp chunks of whole mask words
-    const int nwords = (F + 31) >> 5, nw = blockDim.x >> 5;
-    const int wchunk = (nwords + nw - 1) / nw;
-    const int w0 = min(nwords, warp * wchunk), w1 = min(nwords, w0 + wchunk);
-    int gt = 0, eq = 0;
-    for (int w = w0; w < w1; ++w) {
-        const int j = 32 * w + lane;
-        const uint32_t kv = j < F ? key[j] : 0u;
-        gt += __popc(__ballot_sync(0xffffffffu, j < F && kv > T));
-        eq += __popc(__ballot_sync(0xffffffffu, j < F && kv == T));
-    }
-    int tot;
-    const int eq_base = __shfl_sync(0xffffffffu, block_excl_scan(lane == 0 ? eq : 0, tmp, &tot), 0);
-    const int eq_take = (int)min((unsigned)eq, take_eq > (unsigned)eq_base ? take_eq - (unsigned)eq_base : 0u);
-    int pos = __shfl_sync(0xffffffffu, block_excl_scan(lane == 0 ? gt + eq_take : 0, tmp, &tot), 0);
-    int eq_seen = eq_base;
-    const unsigned lt = (1u << lane) - 1u;
     const bool want_h = a.lh && a.nb == 1;  // h_j = a_j * u_j for the selected neurons
     float *aeff = a.aeff + (size_t)b * F;
     int32_t *lidx = a.lidx + (size_t)b * F;
     constexpr int U = 4;  // mask words per step: the a_j, u_j loads of a step are issued together
-    for (int w = w0; w < w1; w += U) {
+    for (int w = ch.w0; w < ch.w1; w += U) {
         float av[U], uv[U];
 #pragma unroll
         for (int q = 0; q < U; ++q) {
             const int j = 32 * (w + q) + lane;
-            const bool ld = want_h && w + q < w1 && j < F;
+            const bool ld = want_h && w + q < ch.w1 && j < F;
             av[q] = ld ? aeff[j] : 0.f;
             uv[q] = ld ? a.uval[j] : 0.f;
         }
 #pragma unroll
         for (int q = 0; q < U; ++q) {
-            if (w + q >= w1) break;
+            if (w + q >= ch.w1) break;
             const int j = 32 * (w + q) + lane;
-            const bool ok = j < F;
-            const uint32_t kv = ok ? key[j] : 0u;
-            const bool e = ok && kv == T;
-            const unsigned ebal = __ballot_sync(0xffffffffu, e);
-            const bool sel = ok && (kv > T || (e && (unsigned)(eq_seen + __popc(ebal & lt)) < take_eq));
-            const unsigned sbal = __ballot_sync(0xffffffffu, sel);
-            if (sel) {
-                const int r = pos + __popc(sbal & lt);
-                if (want_h) a.lh[r] = av[q] * uv[q];
-                lidx[r] = j;
-            } else if (ok) {
+            const TopkWord t = topk_word(key, F, forced, cut, w + q, ch);
+            if (t.sel) {
+                if (want_h) a.lh[t.pos] = av[q] * uv[q];
+                lidx[t.pos] = j;
+            } else if (j < F) {
                 aeff[j] = 0.f;
             }
-            if (lane == 0 && a.mask) a.mask[(size_t)b * nwords + w + q] = sbal;
-            pos += __popc(sbal);
-            eq_seen += __popc(ebal);
+            if (lane == 0 && a.mask) a.mask[(size_t)b * nwords + w + q] = t.bal;
         }
     }
-    for (int c = tid; c < a.C; c += blockDim.x) a.cnt[(size_t)b * a.C + c] = c == 0 ? tot : 0;
+    for (int c = tid; c < a.C; c += blockDim.x) a.cnt[(size_t)b * a.C + c] = c == 0 ? ch.total : 0;
 }
 
 // union of the per-token keep-ratio selections (nb > 1), ascending
@@ -1264,6 +1207,9 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
             ka.cnt = cnt;
             ka.lidx = lidx;
             ka.mask = p.nb > 1 ? mask : nullptr;
+            ka.core = c.core;
+            ka.n_core = c.n_core;
+            ka.err = err;
             const size_t ksm = p.F <= kKeepStage ? sizeof(uint32_t) * (size_t)p.F : 0;
             if (ksm && (e = set_max_smem((const void *)k_keep_ratio, (int)(sizeof(uint32_t) * kKeepStage))) !=
                            cudaSuccess)

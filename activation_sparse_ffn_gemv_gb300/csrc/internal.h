@@ -79,6 +79,8 @@ struct DecodeCall {
     int32_t *active_idx, *n_active;
     void *ws;
     float *scores_only;  // non-null: sffn_gate_scores (write scores, nothing else)
+    const int32_t *core; // keep-ratio: the layer's core set (sffn_decode_tiered), or null
+    int n_core;
 };
 
 sffn_status run_decode(const DecodeCall &c, const DecodePlan &p, cudaStream_t s);
@@ -91,6 +93,10 @@ sffn_status run_down_norms(const sffn_ffn_weights *w, float *norms, cudaStream_t
 // One-token finish over per-chunk partials and lists in the workspace (part
 // [C, d], cnt [C], lidx [C, R]): the fixed-order reduction and the list writes.
 sffn_status run_reduce_chunks(const DecodeCall &c, const DecodePlan &p, cudaStream_t s);
+// Core set of a keep-ratio tier from calibration scores (tiers.cu).
+size_t tier_core_workspace(int N, int F);
+sffn_status run_tier_core_set(const float *scores, int N, int F, int k, int c, int32_t *core, void *ws,
+                              cudaStream_t s);
 // Decode with the low-rank gate predictor (predict.cu): one token, bf16 / fp32.
 sffn_status run_decode_predicted(const DecodeCall &c, const DecodePlan &p, const float *factor_a,
                                  const float *factor_b, int rank, float alpha, cudaStream_t s);

@@ -75,6 +75,12 @@ def lib():
         L.sffn_decode_dense.restype = I
         L.sffn_decode_predicted.argtypes = [P, W, P, P, I, F, P, P, P, P, S, P]
         L.sffn_decode_predicted.restype = I
+        L.sffn_decode_tiered.argtypes = [P, I, W, I, F, P, I, P, P, P, P, S, P]
+        L.sffn_decode_tiered.restype = I
+        L.sffn_tier_core_workspace_size.argtypes = [I, I]
+        L.sffn_tier_core_workspace_size.restype = S
+        L.sffn_tier_core_set.argtypes = [P, I, I, I, I, P, P, S, P]
+        L.sffn_tier_core_set.restype = I
         L.sffn_gate_scores.argtypes = [P, I, W, I, P, P, S, P]
         L.sffn_gate_scores.restype = I
         L.sffn_token_select.argtypes = [P, I, I, F, I, I, P, P, P, S, P]
@@ -216,6 +222,44 @@ def decode_predicted(x: torch.Tensor, w: Weights, factor_a, factor_b, alpha: flo
                                      _ptr(n_active), _ptr(workspace), workspace.numel(), _stream(stream))
     _check(st, "sffn_decode_predicted")
     return out, active_idx, n_active
+
+
+def decode_tiered(x: torch.Tensor, w: Weights, score: int, keep_ratio: float, core=None, out=None,
+                  active_idx=None, n_active=None, workspace=None, stream=None):
+    """Keep-ratio decode with a core set (int32 device tensor of column
+    indices, ascending; None: no core).  Returns (out, active_idx, n_active)."""
+    B = x.shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    if active_idx is None:
+        active_idx = torch.empty((B, w.d_ff), dtype=torch.int32, device=x.device)
+    if n_active is None:
+        n_active = torch.empty(B, dtype=torch.int32, device=x.device)
+    if workspace is None:
+        workspace = alloc_workspace(WS_DECODE, B, w, x.device)
+    nc = 0 if core is None else int(core.numel())
+    st = lib().sffn_decode_tiered(_ptr(x), B, w.ref(), int(score), float(keep_ratio), _ptr(core), nc, _ptr(out),
+                                  _ptr(active_idx), _ptr(n_active), _ptr(workspace), workspace.numel(),
+                                  _stream(stream))
+    _check(st, "sffn_decode_tiered")
+    return out, active_idx, n_active
+
+
+def tier_core_set(calib_scores: torch.Tensor, k: int, n_core: int, core=None, workspace=None, stream=None):
+    """Core set of a keep-ratio tier from calibration scores [N, d_ff] (fp32,
+    device): int32 [n_core], ascending."""
+    N, F = calib_scores.shape
+    if core is None:
+        core = torch.empty(n_core, dtype=torch.int32, device=calib_scores.device)
+    if workspace is None:
+        nb = lib().sffn_tier_core_workspace_size(N, F)
+        if nb == 0:
+            raise SffnError(ERR_SHAPE, "sffn_tier_core_workspace_size")
+        workspace = torch.empty(nb, dtype=torch.uint8, device=calib_scores.device)
+    st = lib().sffn_tier_core_set(_ptr(calib_scores), N, F, int(k), int(n_core), _ptr(core), _ptr(workspace),
+                                  workspace.numel(), _stream(stream))
+    _check(st, "sffn_tier_core_set")
+    return core
 
 
 def decode_noalloc(x: torch.Tensor, w: Weights, mode: int, score: int = SCORE_GATE, param: float = 0.0,

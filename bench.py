@@ -474,6 +474,41 @@ def bench_decode_sweeps(args, dev, T=256):
         kr[name] = by
     out["keep_ratio"] = {"workload": "qwen2.5-3b-swiglu: d_model 2048, d_ff 11008 bf16, 36 layers, keep the "
                                      "top d_ff/M scores, B=1", "by_score": kr}
+
+    # ---- tier tables (sffn_decode_tiered): per layer a core of half the tier
+    # from 64 calibration tokens (sffn_tier_core_set), the rest chosen online
+    xc = W.make_tokens(3, 64, seed=99, device=dev)
+    tiers = {}
+    for name, score in (("gate_up", sffn.SCORE_GATE_UP), ("gate", sffn.SCORE_GATE)):
+        by = {}
+        for M in (4, 8):
+            k = max(1, int(F / M))
+            t0 = torch.cuda.Event(enable_timing=True)
+            t1 = torch.cuda.Event(enable_timing=True)
+            cores = []
+            for l, w in enumerate(ws):
+                sc = torch.cat([sffn.gate_scores(xc[i:i + 8], w, score) for i in range(0, 64, 8)])
+                if l == 0:
+                    t0.record()
+                cores.append(sffn.tier_core_set(sc, k, k // 2))
+                if l == 0:
+                    t1.record()
+            torch.cuda.synchronize()
+
+            def enq():
+                for t in range(T):
+                    sffn.decode_tiered(x[t:t + 1], ws[t % c["layers"]], score, 1.0 / M, cores[t % c["layers"]],
+                                       out=bufs["o"][t:t + 1], active_idx=bufs["idx"][t:t + 1],
+                                       n_active=bufs["n"][t:t + 1], workspace=bufs["work"], stream=stream)
+            us = _time_graph(enq, stream, max(3, args.steps // 3), args.warmup) * 1e3 / T
+            a = float(bufs["n"][:T].float().mean().item()) / F
+            nb = F * r * ((2 + a) if score == sffn.SCORE_GATE_UP else (1 + 2 * a))
+            by[str(M)] = point(us, nb, a=round(a, 4), core=k // 2,
+                               speedup_vs_keep_ratio=round(kr[name][str(M)]["us_per_token"] / us, 3),
+                               core_set_ms=round(t0.elapsed_time(t1), 4))
+        tiers[name] = by
+    out["tiered"] = {"workload": "as keep_ratio, with a per-layer core of k/2 columns from 64 calibration tokens; "
+                                 "core_set_ms: sffn_tier_core_set for one layer (offline)", "by_score": tiers}
     del layers, ws, x, bufs
     torch.cuda.empty_cache()
 

@@ -172,6 +172,41 @@ sffn_status sffn_decode_predicted(const void *x, const sffn_ffn_weights *w, cons
                                   const float *factor_b, int rank, float alpha, void *out, int32_t *active_idx,
                                   int32_t *n_active, void *workspace, size_t ws_bytes, sffn_stream_t stream);
 
+/* Keep-ratio decode with a per-layer core set (WiSparse write-up, sec. 2.2,
+ * the paragraph after the score definition: the columns kept most often at a
+ * tier form a guaranteed base set, and each token completes its selection
+ * dynamically; sec. 5 FAQ: batch > 1 shares one tier).  Per token:
+ *   keep = core  U  the (k - |core|) largest scores among the columns outside
+ *          the core (ties to the lower index), k = max(1, floor(d_ff * keep_ratio));
+ * with |core| >= k the token keeps the core alone.  Arguments and results as
+ * sffn_decode in SFFN_MODE_KEEP_RATIO (B tokens: the union of their sets is
+ * read once, each token masked to its own set), plus
+ *   core_idx   [n_core] int32 device array: the core's columns (ascending,
+ *              distinct, as sffn_tier_core_set writes them); an index outside
+ *              [0, d_ff) is skipped and recorded as SFFN_ERR_DEVICE in the
+ *              workspace's error word (sffn_read_device_error).
+ *   n_core     0 <= n_core <= d_ff (0: the plain keep-ratio selection).
+ * bf16 / fp32 weights (int4-g64: SFFN_ERR_UNSUPPORTED, as keep-ratio). */
+sffn_status sffn_decode_tiered(const void *x, int B, const sffn_ffn_weights *w, int score, float keep_ratio,
+                               const int32_t *core_idx, int n_core, void *out, int32_t *active_idx, int32_t *n_active,
+                               void *workspace, size_t ws_bytes, sffn_stream_t stream);
+
+/* Bytes of workspace for sffn_tier_core_set (0 for an invalid request). */
+size_t sffn_tier_core_workspace_size(int n_calib, int d_ff);
+
+/* The core set of a keep-ratio tier from calibration scores (WiSparse
+ * write-up, sec. 2.2): for each calibration token its top-k columns (the k
+ * largest scores, ties to the lower index); per column the number of tokens
+ * that kept it; the core is the n_core columns with the largest counts (count
+ * ties to the lower index), written ascending to core_idx [n_core].
+ *   calib_scores [n_calib, d_ff] fp32 device array of non-negative scores (as
+ *                sffn_gate_scores writes them); 1 <= n_calib <= 65536.
+ *   k            the tier's k, 1 <= k <= d_ff; 0 <= n_core <= d_ff (core_idx may be
+ *                NULL when n_core is 0).
+ *   workspace    sffn_tier_core_workspace_size(n_calib, d_ff) bytes. */
+sffn_status sffn_tier_core_set(const float *calib_scores, int n_calib, int d_ff, int k, int n_core, int32_t *core_idx,
+                               void *workspace, size_t ws_bytes, sffn_stream_t stream);
+
 /* Size of the scratch array built into the library for sffn_decode_noalloc. */
 #define SFFN_NOALLOC_SCRATCH_BYTES (4u << 20)
 

@@ -177,6 +177,43 @@ def test_predicted_decode_argument_checks(S):
     assert pred(wts(), fa=None, fb=None, rank=0, alpha=inf) not in (S.ERR_INVALID_ARG, S.ERR_SHAPE)
 
 
+def test_tier_entry_points_argument_checks(S):
+    L = S.lib()
+
+    def wts(**kw):
+        f = dict(wdtype=S.BF16, act=S.ACT_SILU, d_model=64, d_ff=128)
+        f.update(kw)
+        return S.FFNWeights(f["wdtype"], f["act"], f["d_model"], f["d_ff"], 16, 16, 16, 16, 16, 16, None, 16)
+
+    def tiered(w, B=1, score=0, ratio=0.25, core=16, nc=4, x=16, out=16):
+        return L.sffn_decode_tiered(x, B, C.byref(w), score, ratio, core, nc, out, 16, 16, 256, 1 << 20, None)
+
+    assert tiered(wts(), x=None) == S.ERR_INVALID_ARG
+    assert tiered(wts(), ratio=0.0) == S.ERR_INVALID_ARG
+    assert tiered(wts(), ratio=1.5) == S.ERR_INVALID_ARG
+    assert tiered(wts(), B=9) == S.ERR_SHAPE
+    assert tiered(wts(wdtype=S.INT4_G64, d_model=512)) == S.ERR_UNSUPPORTED
+    # the core is checked after the call's own arguments (on a machine without
+    # a GPU those end at the device check)
+    assert tiered(wts(), nc=-1) in (S.ERR_SHAPE, S.ERR_CUDA)
+    assert tiered(wts(), core=None) in (S.ERR_INVALID_ARG, S.ERR_CUDA)
+
+    def core_set(scores=16, N=4, F=128, k=16, c=8, core=16):
+        return L.sffn_tier_core_set(scores, N, F, k, c, core, 256, 1 << 20, None)
+
+    assert core_set(scores=None) == S.ERR_INVALID_ARG
+    assert core_set(core=None) == S.ERR_INVALID_ARG
+    assert core_set(N=0) == S.ERR_SHAPE
+    assert core_set(F=70000) == S.ERR_SHAPE
+    assert core_set(k=0) == S.ERR_INVALID_ARG
+    assert core_set(k=129) == S.ERR_INVALID_ARG
+    assert core_set(c=-1) == S.ERR_INVALID_ARG
+    assert core_set(c=129) == S.ERR_INVALID_ARG
+    assert L.sffn_tier_core_workspace_size(0, 128) == 0
+    assert L.sffn_tier_core_workspace_size(4, 0) == 0
+    assert L.sffn_tier_core_workspace_size(4, 128) > 0
+
+
 @pytest.mark.gpu
 def test_workspace_checks_on_gpu(S):
     from activation_sparse_ffn_gemv_gb300 import workloads as W
