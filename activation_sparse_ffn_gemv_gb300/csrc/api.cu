@@ -311,6 +311,68 @@ sffn_status sffn_tier_core_set(const float *calib_scores, int n_calib, int d_ff,
     return st;
 }
 
+int sffn_moe_progressive_k(int layer) {
+    // depth ranges and their expert counts; past the last range its count holds
+    static const int kRanges[3][3] = {{0, 15, 6}, {16, 39, 5}, {40, 60, 4}};
+    if (layer < 0) return -1;
+    for (const auto &r : kRanges)
+        if (layer >= r[0] && layer <= r[1]) return r[2];
+    return kRanges[2][2];
+}
+
+sffn_status sffn_moe_route(const float *logits, int T, int E, int cap, float mass, const int32_t *buckets,
+                           int n_buckets, int kmax, int32_t *k_out, int32_t *experts, float *weights,
+                           sffn_stream_t stream) {
+    if (!logits || !k_out || !experts || !weights || !buckets) return SFFN_ERR_INVALID_ARG;
+    if (T < 0 || E < 1 || E > kMoeMaxExperts) return SFFN_ERR_SHAPE;
+    if (cap < 1 || cap > E || cap > kMoeMaxK || kmax < cap || kmax > kMoeMaxK) return SFFN_ERR_SHAPE;
+    if (n_buckets < 1 || n_buckets > kMoeMaxBuckets || !(mass == mass)) return SFFN_ERR_INVALID_ARG;
+    MoeRouteArgs a = {};
+    for (int i = 0; i < n_buckets; ++i) {
+        if (buckets[i] < 1 || buckets[i] > kMoeMaxK || (i > 0 && buckets[i] <= buckets[i - 1]))
+            return SFFN_ERR_INVALID_ARG;
+        a.buckets[i] = buckets[i];
+    }
+    if (device_sm_count() <= 0) return SFFN_ERR_CUDA;
+    if (T == 0) return SFFN_OK;
+    a.logits = logits;
+    a.T = T;
+    a.E = E;
+    a.cap = cap;
+    a.kmax = kmax;
+    a.mass = mass;
+    a.n_buckets = n_buckets;
+    a.k_out = k_out;
+    a.experts = experts;
+    a.weights = weights;
+    sffn_status st = run_moe_route(a, (cudaStream_t)stream);
+    if (st == SFFN_OK) st = cuda_status(cudaGetLastError());
+    return st;
+}
+
+size_t sffn_moe_budget_workspace_size(int L, int d_model) {
+    if (L < 1 || L > (1 << 20) || d_model < 8 || d_model > 65536 || d_model % 8 != 0) return 0;
+    return moe_budget_workspace(L, d_model);
+}
+
+sffn_status sffn_moe_block_budget(const void *y_attn, int L, int d_model, float mass, float min_ratio,
+                                  float max_ratio, int block, int32_t *token_idx, int32_t *n_tokens, int32_t *ranges,
+                                  int32_t *n_ranges, void *workspace, size_t ws_bytes, sffn_stream_t stream) {
+    if (!y_attn || !token_idx || !n_tokens || !ranges || !n_ranges) return SFFN_ERR_INVALID_ARG;
+    if (L < 1 || L > (1 << 20) || d_model < 8 || d_model > 65536 || d_model % 8 != 0) return SFFN_ERR_SHAPE;
+    if (block < 1 || (L + block - 1) / block > kMoeMaxBlocks) return SFFN_ERR_SHAPE;
+    if (!(mass == mass) || !(min_ratio >= 0.f) || !(max_ratio <= 1.f) || !(min_ratio <= max_ratio))
+        return SFFN_ERR_INVALID_ARG;
+    if (!aligned16(y_attn)) return SFFN_ERR_ALIGNMENT;
+    if (device_sm_count() <= 0) return SFFN_ERR_CUDA;
+    sffn_status st = check_ws(workspace, ws_bytes, moe_budget_workspace(L, d_model));
+    if (st != SFFN_OK) return st;
+    st = run_moe_block_budget(y_attn, L, d_model, mass, min_ratio, max_ratio, block, token_idx, n_tokens, ranges,
+                              n_ranges, workspace, (cudaStream_t)stream);
+    if (st == SFFN_OK) st = cuda_status(cudaGetLastError());
+    return st;
+}
+
 sffn_status sffn_gate_scores(const void *x, int B, const sffn_ffn_weights *w, int score, float *scores,
                              void *workspace, size_t ws_bytes, sffn_stream_t stream) {
     sffn_status st = check_decode_args(x, B, w, SFFN_MODE_THRESHOLD, score, 0.f);

@@ -97,6 +97,25 @@ sffn_status run_reduce_chunks(const DecodeCall &c, const DecodePlan &p, cudaStre
 size_t tier_core_workspace(int N, int F);
 sffn_status run_tier_core_set(const float *scores, int N, int F, int k, int c, int32_t *core, void *ws,
                               cudaStream_t s);
+// MoE routing and block budget (moe.cu).
+constexpr int kMoeMaxExperts = 512;   // router width
+constexpr int kMoeMaxK = 8;           // experts per token
+constexpr int kMoeMaxBlocks = 8192;   // budget blocks per sequence
+constexpr int kMoeMaxBuckets = 8;
+struct MoeRouteArgs {
+    const float *logits;  // [T, E]
+    int T, E, cap, kmax;
+    float mass;
+    int n_buckets;
+    int buckets[kMoeMaxBuckets];  // ascending
+    int32_t *k_out, *experts;     // [T], [T, kmax]
+    float *weights;               // [T, kmax]
+};
+sffn_status run_moe_route(const MoeRouteArgs &a, cudaStream_t s);
+size_t moe_budget_workspace(int L, int d);
+sffn_status run_moe_block_budget(const void *y_attn, int L, int d, float mass, float min_ratio, float max_ratio,
+                                 int block, int32_t *token_idx, int32_t *n_tokens, int32_t *ranges,
+                                 int32_t *n_ranges, void *ws, cudaStream_t s);
 // Decode with the low-rank gate predictor (predict.cu): one token, bf16 / fp32.
 sffn_status run_decode_predicted(const DecodeCall &c, const DecodePlan &p, const float *factor_a,
                                  const float *factor_b, int rank, float alpha, cudaStream_t s);

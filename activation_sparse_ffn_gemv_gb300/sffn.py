@@ -81,6 +81,14 @@ def lib():
         L.sffn_tier_core_workspace_size.restype = S
         L.sffn_tier_core_set.argtypes = [P, I, I, I, I, P, P, S, P]
         L.sffn_tier_core_set.restype = I
+        L.sffn_moe_progressive_k.argtypes = [I]
+        L.sffn_moe_progressive_k.restype = I
+        L.sffn_moe_route.argtypes = [P, I, I, I, F, C.POINTER(C.c_int32), I, I, P, P, P, P]
+        L.sffn_moe_route.restype = I
+        L.sffn_moe_budget_workspace_size.argtypes = [I, I]
+        L.sffn_moe_budget_workspace_size.restype = S
+        L.sffn_moe_block_budget.argtypes = [P, I, I, F, F, F, I, P, P, P, P, P, S, P]
+        L.sffn_moe_block_budget.restype = I
         L.sffn_gate_scores.argtypes = [P, I, W, I, P, P, S, P]
         L.sffn_gate_scores.restype = I
         L.sffn_token_select.argtypes = [P, I, I, F, I, I, P, P, P, S, P]
@@ -260,6 +268,57 @@ def tier_core_set(calib_scores: torch.Tensor, k: int, n_core: int, core=None, wo
                                   workspace.numel(), _stream(stream))
     _check(st, "sffn_tier_core_set")
     return core
+
+
+def moe_progressive_k(layer: int) -> int:
+    return int(lib().sffn_moe_progressive_k(int(layer)))
+
+
+def moe_route(logits: torch.Tensor, cap: int, mass: float = 0.5, buckets=(3, 4, 5, 6), kmax=None, k_out=None,
+              experts=None, weights=None, stream=None):
+    """Adaptive expert top-K: (K [T], experts [T, kmax] ascending then -1,
+    weights [T, kmax])."""
+    T, E = logits.shape
+    kmax = cap if kmax is None else kmax
+    dev = logits.device
+    if k_out is None:
+        k_out = torch.empty(T, dtype=torch.int32, device=dev)
+    if experts is None:
+        experts = torch.empty((T, kmax), dtype=torch.int32, device=dev)
+    if weights is None:
+        weights = torch.empty((T, kmax), dtype=torch.float32, device=dev)
+    bk = (C.c_int32 * len(buckets))(*buckets)
+    st = lib().sffn_moe_route(_ptr(logits), T, E, int(cap), float(mass), bk, len(buckets), int(kmax), _ptr(k_out),
+                              _ptr(experts), _ptr(weights), _stream(stream))
+    _check(st, "sffn_moe_route")
+    return k_out, experts, weights
+
+
+def moe_block_budget(y_attn: torch.Tensor, mass: float, min_ratio: float = 0.10, max_ratio: float = 0.50,
+                     block: int = 128, token_idx=None, n_tokens=None, ranges=None, n_ranges=None, workspace=None,
+                     stream=None):
+    """Block token budget: (token_idx [L], n_tokens [1], ranges [nblocks, 2], n_ranges [1])."""
+    L, d = y_attn.shape
+    dev = y_attn.device
+    nblocks = (L + block - 1) // block
+    if token_idx is None:
+        token_idx = torch.empty(L, dtype=torch.int32, device=dev)
+    if n_tokens is None:
+        n_tokens = torch.empty(1, dtype=torch.int32, device=dev)
+    if ranges is None:
+        ranges = torch.empty((nblocks, 2), dtype=torch.int32, device=dev)
+    if n_ranges is None:
+        n_ranges = torch.empty(1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        nb = lib().sffn_moe_budget_workspace_size(L, d)
+        if nb == 0:
+            raise SffnError(ERR_SHAPE, "sffn_moe_budget_workspace_size")
+        workspace = torch.empty(nb, dtype=torch.uint8, device=dev)
+    st = lib().sffn_moe_block_budget(_ptr(y_attn), L, d, float(mass), float(min_ratio), float(max_ratio), int(block),
+                                     _ptr(token_idx), _ptr(n_tokens), _ptr(ranges), _ptr(n_ranges), _ptr(workspace),
+                                     workspace.numel(), _stream(stream))
+    _check(st, "sffn_moe_block_budget")
+    return token_idx, n_tokens, ranges, n_ranges
 
 
 def decode_noalloc(x: torch.Tensor, w: Weights, mode: int, score: int = SCORE_GATE, param: float = 0.0,

@@ -293,6 +293,7 @@ def run_ours(args):
         if rank == 0:
             res["prefill"] = pf
             res["prefill_stack"] = bench_prefill_stack(args, dev)
+            res["moe"] = bench_moe(args, dev)
     if not args.no_sweeps:
         sw = bench_decode_sweeps(args, dev)
         if rank == 0:
@@ -313,7 +314,8 @@ def run_prefill_only(args):
     res = bench_prefill(args, torch.device("cuda", local), rank, 1, None)
     if rank != 0:
         return None
-    return {"prefill": res, "prefill_stack": bench_prefill_stack(args, torch.device("cuda", local))}
+    return {"prefill": res, "prefill_stack": bench_prefill_stack(args, torch.device("cuda", local)),
+            "moe": bench_moe(args, torch.device("cuda", local))}
 
 
 def _time_graph(enqueue, stream, steps, warmup):
@@ -582,6 +584,55 @@ def traffic_for(key):
         return e["bytes"] if h.hexdigest() == e["sha256"] else None
     except Exception:
         return None
+
+
+def bench_moe(args, dev):
+    """MoE routing and block budget on the prefill workload's sequence: the
+    adaptive top-K of 16384 tokens over 384 routed experts (a layer of the
+    16-39 range: cap 5), and the 128-token block budget of the L 16384,
+    d_model 5120 sequence at mass 0.5."""
+    import torch
+
+    from activation_sparse_ffn_gemv_gb300 import sffn
+    from activation_sparse_ffn_gemv_gb300 import workloads as W
+    hbm, _, _, _ = peaks()
+    T, E = 16384, 384
+    g = torch.Generator(device=dev).manual_seed(3)
+    logits = [torch.randn(T, E, generator=g, device=dev) * 1.5 for _ in range(4)]  # 4 x 25 MB: beyond L2
+    cap = sffn.moe_progressive_k(20)
+    k = torch.empty(T, dtype=torch.int32, device=dev)
+    ex = torch.empty((T, cap), dtype=torch.int32, device=dev)
+    wt = torch.empty((T, cap), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize()
+
+    def enq():
+        for i in range(4):
+            sffn.moe_route(logits[i], cap, 0.5, k_out=k, experts=ex, weights=wt, stream=stream)
+    ms = _time_graph(enq, stream, max(5, args.steps), args.warmup) / 4
+    nbytes = T * E * 4 + T * (4 + 8 * cap)
+    gbps = nbytes / (ms * 1e-3) / 1e9
+    route = {"workload": f"{T} tokens x {E} routed experts fp32 logits, layer 20 (cap {cap}), buckets (3,4,5,6), "
+                         "mass 0.5", "ms": round(ms, 4), "gbps": round(gbps, 1), "frac_hbm": round(gbps / hbm, 4),
+             "mean_k": round(float(k.float().mean().item()), 3)}
+    c = W.CONFIGS[5]
+    L, d = c["L"], c["d_model"]
+    _, Ya = W.make_prefill_inputs(L, d, seed=0, device=dev)
+    nb = (L + 127) // 128
+    ti = torch.empty(L, dtype=torch.int32, device=dev)
+    nt = torch.empty(1, dtype=torch.int32, device=dev)
+    rg = torch.empty((nb, 2), dtype=torch.int32, device=dev)
+    nr = torch.empty(1, dtype=torch.int32, device=dev)
+    wsb = torch.empty(sffn.lib().sffn_moe_budget_workspace_size(L, d), dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    def enq2():
+        sffn.moe_block_budget(Ya, 0.5, token_idx=ti, n_tokens=nt, ranges=rg, n_ranges=nr, workspace=wsb,
+                              stream=stream)
+    ms2 = _time_graph(enq2, stream, max(5, args.steps), args.warmup)
+    budget = {"workload": f"L {L}, d_model {d} bf16 attention outputs, mass 0.5, ratios [0.10, 0.50], 128-token "
+                          "blocks", "ms": round(ms2, 4), "tokens": int(nt.item()), "ranges": int(nr.item())}
+    return {"route": route, "block_budget": budget}
 
 
 def bench_prefill_stack(args, dev):

@@ -207,6 +207,45 @@ size_t sffn_tier_core_workspace_size(int n_calib, int d_ff);
 sffn_status sffn_tier_core_set(const float *calib_scores, int n_calib, int d_ff, int k, int n_core, int32_t *core_idx,
                                void *workspace, size_t ws_bytes, sffn_stream_t stream);
 
+/* ---- MoE layers (RedKnot write-up, bhfrc.com/news/43276, section "adaptive
+ * expert Top-K") ---- */
+
+/* The progressive top-K by depth: 6 experts for layers 0-15, 5 for 16-39, 4 for
+ * 40-60 (and past 60); -1 for a negative layer. */
+int sffn_moe_progressive_k(int layer);
+
+/* Adaptive expert top-K for T tokens.  Per token (logits [T, E] fp32, device):
+ * probabilities p = softmax(logits) (fp32); experts ranked by probability
+ * descending, ties to the lower expert index; K = the smallest bucket b (from
+ * buckets[0..n_buckets), ascending, host memory) with b <= cap whose top-b mass
+ * reaches `mass` (the page's default 0.50), else cap (the layer's progressive
+ * K).  Writes k_out [T], experts [T, kmax] (the K experts ascending, then -1)
+ * and weights [T, kmax] (their probabilities renormalised to sum 1, then 0).
+ * 1 <= E <= 512, 1 <= cap <= min(E, 8), cap <= kmax <= 8, bucket values in
+ * [1, 8].  Nothing is allocated; T = 0 is a no-op. */
+sffn_status sffn_moe_route(const float *logits, int T, int E, int cap, float mass, const int32_t *buckets,
+                           int n_buckets, int kmax, int32_t *k_out, int32_t *experts, float *weights,
+                           sffn_stream_t stream);
+
+/* Bytes of workspace for sffn_moe_block_budget (0 for an invalid request). */
+size_t sffn_moe_budget_workspace_size(int L, int d_model);
+
+/* The block token budget of an MoE layer over one sequence, on the GPU with no
+ * host synchronisation.  A token's importance is the L2 norm of its attention
+ * output row (y_attn [L, d_model] bf16, as sffn_token_select); f = the share of
+ * tokens the mass rule keeps (sffn_token_select with this mass, no recent tail,
+ * no minimum) clamped to [min_ratio, max_ratio] (the page's 0.10 / 0.50);
+ * nsel = max(1, ceil(f * nblocks)) of the nblocks = ceil(L / block) blocks of
+ * `block` consecutive tokens (the page's 128), those with the largest summed
+ * importance (ties to the lower block index), run the MoE.  Writes
+ * token_idx [L] (the chosen blocks' tokens ascending, first *n_tokens entries)
+ * and ranges [2 * nblocks] (the *n_ranges maximal contiguous [start, end) token
+ * ranges, ascending).  The list feeds sffn_prefill's sel_idx / n_sel as it is.
+ * nblocks <= 8192; workspace sffn_moe_budget_workspace_size(L, d_model) bytes. */
+sffn_status sffn_moe_block_budget(const void *y_attn, int L, int d_model, float mass, float min_ratio,
+                                  float max_ratio, int block, int32_t *token_idx, int32_t *n_tokens, int32_t *ranges,
+                                  int32_t *n_ranges, void *workspace, size_t ws_bytes, sffn_stream_t stream);
+
 /* Size of the scratch array built into the library for sffn_decode_noalloc. */
 #define SFFN_NOALLOC_SCRATCH_BYTES (4u << 20)
 
