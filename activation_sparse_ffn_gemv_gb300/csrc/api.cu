@@ -118,7 +118,6 @@ sffn_status check_decode_args(const void *x, int B, const sffn_ffn_weights *w, i
     if (mode == SFFN_MODE_THRESHOLD && !(param >= 0.f) ) return SFFN_ERR_INVALID_ARG;
     if (mode == SFFN_MODE_KEEP_RATIO && !(param > 0.f && param <= 1.f)) return SFFN_ERR_INVALID_ARG;
     if (w->wdtype == SFFN_INT4_G64) {
-        if (mode == SFFN_MODE_KEEP_RATIO) return SFFN_ERR_UNSUPPORTED;
         if (w->d_model % 512 != 0) return SFFN_ERR_SHAPE;  // a row's scales: a 16-byte multiple
     }
     return SFFN_OK;

@@ -27,6 +27,13 @@ SFFN_DEV uint4 ldg_stream(const void *p) {
     return r;
 }
 
+// 32-bit streaming load (read once; no L1 allocation).
+SFFN_DEV uint32_t ldg_stream_u32(const void *p) {
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(p));
+    return r;
+}
+
 SFFN_DEV uint4 ldg_v4(const void *p) {
     uint4 r;
     asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"

@@ -654,6 +654,7 @@ __global__ void __launch_bounds__(kSelThreads) k_union(const uint32_t *mask, int
 
 struct UpDownArgs {
     const void *wu, *wdT;
+    const void *su, *sdT;      // int4: fp16 group scales of W_up / W_downT rows
     const void *x;
     int d, F, nb, R, C, list_u;
     const int *cnt, *lidx;
@@ -670,8 +671,7 @@ constexpr int kUpDownMaxThreads = 512;   // d_model <= 4096 at 8 columns per thr
 
 template <class W, int NB, bool HAVE_U>
 __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
-    constexpr int COLS = 8;                 // output columns per thread
-    constexpr int UPT = COLS / W::E;        // 16-byte units per thread per row
+    constexpr int COLS = 8;                 // output columns per thread (load_row8)
     constexpr int RB = NB <= 2 ? 8 : 4;     // rows per group (loads in flight)
     extern __shared__ float smf[];
     float *xs = smf;                                              // [NB][d] fp32
@@ -731,24 +731,23 @@ __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
     const size_t row_bytes = (size_t)d * 16 / W::E;
     for (int g0 = 0; g0 < nr; g0 += RB) {
         const int ng = min(RB, nr - g0);
-        uint4 dn[RB][UPT], up[HAVE_U ? 1 : RB][UPT];
+        Row8 dn[RB], up[HAVE_U ? 1 : RB];
+        float ds[RB], us[HAVE_U ? 1 : RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
+            dn[r] = Row8{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+            ds[r] = 0.f;
+            if (!HAVE_U) {
+                up[HAVE_U ? 0 : r] = dn[r];
+                us[HAVE_U ? 0 : r] = 0.f;
+            }
             if (r < ng && own) {
                 const int j = srow[g0 + r];
-                const char *pd = static_cast<const char *>(a.wdT) + (size_t)j * row_bytes + (size_t)col0 * 16 / W::E;
-#pragma unroll
-                for (int q = 0; q < UPT; ++q) dn[r][q] = ldg_stream(pd + q * 16);
+                dn[r] = load_row8<W>(static_cast<const char *>(a.wdT) + (size_t)j * row_bytes, col0);
+                ds[r] = row_scale8<W>(a.sdT, (size_t)j, d, col0);
                 if (!HAVE_U) {
-                    const char *pu = static_cast<const char *>(a.wu) + (size_t)j * row_bytes + (size_t)col0 * 16 / W::E;
-#pragma unroll
-                    for (int q = 0; q < UPT; ++q) up[HAVE_U ? 0 : r][q] = ldg_stream(pu + q * 16);
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < UPT; ++q) {
-                    dn[r][q] = make_uint4(0, 0, 0, 0);
-                    if (!HAVE_U) up[HAVE_U ? 0 : r][q] = make_uint4(0, 0, 0, 0);
+                    up[HAVE_U ? 0 : r] = load_row8<W>(static_cast<const char *>(a.wu) + (size_t)j * row_bytes, col0);
+                    us[HAVE_U ? 0 : r] = row_scale8<W>(a.su, (size_t)j, d, col0);
                 }
             }
         }
@@ -756,8 +755,7 @@ __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
 #pragma unroll
             for (int r = 0; r < RB; ++r) {
                 float fu[COLS];
-#pragma unroll
-                for (int q = 0; q < UPT; ++q) W::unpack(up[HAVE_U ? 0 : r][q], fu + q * W::E);
+                unpack_row8<W>(up[HAVE_U ? 0 : r], us[HAVE_U ? 0 : r], fu);
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
                     float s = 0.f;
@@ -798,8 +796,7 @@ __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
             float fd[COLS];
-#pragma unroll
-            for (int q = 0; q < UPT; ++q) W::unpack(dn[r][q], fd + q * W::E);
+            unpack_row8<W>(dn[r], ds[r], fd);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
                 const float h = sh[r][b];
@@ -834,6 +831,7 @@ __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
 
 struct DownArgs {
     const void *wdT;
+    const void *sdT;           // int4: fp16 group scales of the W_downT rows
     int d, F, nb, R, C, list_u;
     int by_chunk;              // 1: CTA c walks gate chunk c (grid == C); 0: equal shares of the list
     int max_rows;              // capacity of the row list in shared memory
@@ -848,8 +846,7 @@ constexpr int kDownMaxThreads = 512;
 
 template <class W, int NB>
 __global__ void __launch_bounds__(kDownMaxThreads) k_down(DownArgs a) {
-    constexpr int COLS = 8;
-    constexpr int UPT = COLS / W::E;
+    constexpr int COLS = 8;  // output columns per thread (load_row8)
     constexpr int RB = NB <= 2 ? 16 : 8;
     extern __shared__ int smi[];
     int *coff = smi;                                   // [C + 1]
@@ -916,17 +913,16 @@ __global__ void __launch_bounds__(kDownMaxThreads) k_down(DownArgs a) {
     // all threads run the same control flow (the scan below has barriers);
     // threads beyond the last column only skip their loads and stores
     for (int g0 = 0; g0 < nr; g0 += RB) {
-        uint4 dn[RB][UPT];
+        Row8 dn[RB];
+        float ds[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
+            dn[r] = Row8{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+            ds[r] = 0.f;
             if (own && g0 + r < nr) {
-                const char *pd = static_cast<const char *>(a.wdT) + (size_t)srow[g0 + r] * row_bytes +
-                                 (size_t)col0 * 16 / W::E;
-#pragma unroll
-                for (int q = 0; q < UPT; ++q) dn[r][q] = ldg_stream(pd + q * 16);
-            } else {
-#pragma unroll
-                for (int q = 0; q < UPT; ++q) dn[r][q] = make_uint4(0, 0, 0, 0);
+                const int j = srow[g0 + r];
+                dn[r] = load_row8<W>(static_cast<const char *>(a.wdT) + (size_t)j * row_bytes, col0);
+                ds[r] = row_scale8<W>(a.sdT, (size_t)j, d, col0);
             }
         }
         if (a.by_chunk && g0 == 0) {
@@ -944,8 +940,7 @@ __global__ void __launch_bounds__(kDownMaxThreads) k_down(DownArgs a) {
         for (int r = 0; r < RB; ++r) {
             if (g0 + r < nr) {
                 float fd[COLS];
-#pragma unroll
-                for (int q = 0; q < UPT; ++q) W::unpack(dn[r][q], fd + q * W::E);
+                unpack_row8<W>(dn[r], ds[r], fd);
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
                     const float h = shv[(g0 + r) * NB + b];
@@ -1189,7 +1184,7 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
         nparts = p.C;
         list_ctas = true;
     }
-    if constexpr (W::E <= 8) {  // keep-ratio paths: fp32 / bf16 weights
+    {
         bool have_h = up;  // keep-ratio: h_j known before the down pass
         if (keep) {
             KeepArgs ka = {};
@@ -1230,6 +1225,7 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
         } else if (have_h) {
             DownArgs da = {};
             da.wdT = w->w_downT;
+            da.sdT = w->s_downT;
             da.d = p.d;
             da.F = p.F;
             da.nb = p.nb;
@@ -1251,6 +1247,8 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
             UpDownArgs ua = {};
             ua.wu = w->w_up;
             ua.wdT = w->w_downT;
+            ua.su = w->s_up;
+            ua.sdT = w->s_downT;
             ua.x = c.x;
             ua.d = p.d;
             ua.F = p.F;
@@ -1270,8 +1268,6 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
             if (e == cudaSuccess) e = launch_k(k_updown<W, NB, false>, dim3(p.G2), dim3(threads), smem, s, ua);
         }
         if (e != cudaSuccess) return e;
-    } else {
-        if (keep) return cudaErrorNotSupported;  // rejected by the API for int4
     }
 
     ReduceArgs ra = {};

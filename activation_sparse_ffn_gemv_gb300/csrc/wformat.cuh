@@ -1,6 +1,8 @@
 // wformat.cuh -- stored weight formats of the decode kernels and the staging
 // of the activations in shared memory (sm_103a).
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace sffn {
@@ -72,6 +74,58 @@ struct WINT4 {
     }
 };
 
+// Eight consecutive columns (col0 a multiple of 8) of a stored row, loaded
+// raw: fp32 two 16-byte units, bf16 one, int4 one 32-bit word of 8 codes.
+struct Row8 {
+    uint4 v0, v1;
+};
+
+template <class W>
+SFFN_DEV Row8 load_row8(const void *row, int col0) {
+    const char *p = static_cast<const char *>(row);
+    Row8 r{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if constexpr (W::E == 4) {
+        r.v0 = ldg_stream(p + (size_t)col0 * 4);
+        r.v1 = ldg_stream(p + (size_t)col0 * 4 + 16);
+    } else if constexpr (W::E == 8) {
+        r.v0 = ldg_stream(p + (size_t)col0 * 2);
+    } else {
+        r.v0.x = ldg_stream_u32(p + (size_t)col0 / 2);
+    }
+    return r;
+}
+
+// The row's group scale at col0 (int4: fp16 scales [d/64] per stored row), else 1.
+template <class W>
+SFFN_DEV float row_scale8(const void *scales, size_t row, int d, int col0) {
+    if constexpr (W::Q) {
+        const __half *sr = static_cast<const __half *>(scales) + row * (size_t)(d / 64);
+        return __half2float(sr[col0 / 64]);
+    } else {
+        return 1.f;
+    }
+}
+
+// The eight columns as fp32 (int4: code * scale, exact).
+template <class W>
+SFFN_DEV void unpack_row8(const Row8 &r, float s, float *f) {
+    if constexpr (W::E == 4) {
+        W::unpack(r.v0, f);
+        W::unpack(r.v1, f + 4);
+    } else if constexpr (W::E == 8) {
+        W::unpack(r.v0, f);
+    } else {
+        const uint32_t w = r.v0.x ^ 0x88888888u;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) f[k] = (__uint_as_float(0x4B000000u | ((w >> (4 * k)) & 0xFu)) - 8388616.0f) * s;
+    }
+}
+
+// The format of the activations that go with weights W (fp32 with fp32
+// weights, else bf16).
+template <class W>
+using XFormat = typename std::conditional<sizeof(typename W::X) == 4, WF32, WBF16>::type;
+
 // Copy the activations x [nb, d] into shared memory in their own dtype
 // [NBpad, d] (rows >= nb zero), 128-bit units, four loads in flight per thread.
 template <class W>
@@ -117,7 +171,7 @@ SFFN_DEV void stage_x(float *xs, const void *x, int nb, int NBpad, int d) {
             const int u = base + k * blockDim.x;
             if (u < total) {
                 float f[XE];
-                W::unpack(v[k], f);
+                XFormat<W>::unpack(v[k], f);
                 float4 *dst = reinterpret_cast<float4 *>(xs + (size_t)u * XE);
 #pragma unroll
                 for (int q = 0; q < XE / 4; ++q) dst[q] = make_float4(f[4 * q], f[4 * q + 1], f[4 * q + 2], f[4 * q + 3]);

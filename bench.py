@@ -437,6 +437,14 @@ def bench_decode_sweeps(args, dev, T=256):
                     "|SiLU(g)|*||W_down[:,j]||, B=1",
         "dense": point(dense_us, 3 * F * r, kernel="sffn_decode_dense: every neuron, the three matrices read once"),
         "points": sweep, "breakeven_active_fraction": be}
+    # int4 keep-ratio tiers (gate-and-up score: W_up read in full)
+    kr4 = {}
+    for M in (2, 4, 8):
+        us = run_sparse(ws, x, bufs, 1, sffn.MODE_KEEP_RATIO, sffn.SCORE_GATE_UP, [1.0 / M] * nl)
+        a = float(bufs["n"].float().mean().item()) / F
+        kr4[str(M)] = point(us, F * r * (2 + a), a=round(a, 4), speedup_vs_dense=round(dense_us / us, 3))
+    out["int4_keep_ratio"] = {"workload": "as int4_threshold_sweep, keep the top d_ff/M gate-and-up scores",
+                              "by_M": kr4}
     del layers, ws, x, bufs, sc_ws
     torch.cuda.empty_cache()
 

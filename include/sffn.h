@@ -53,8 +53,7 @@
  *  - Shape limits: d_model % 8 == 0 (fp32/bf16), d_model % 64 == 0 (int4-g64),
  *    8 <= d_model <= 8192, 1 <= d_ff <= 65536, 1 <= B <= 8.  Decode also needs
  *    d_model <= 4096, and for int4-g64 d_model % 512 == 0 (one row's scales are a
- *    multiple of 16 bytes); int4-g64 decode supports the exact and threshold
- *    rules (keep-ratio returns SFFN_ERR_UNSUPPORTED).
+ *    multiple of 16 bytes); int4-g64 decode supports every rule.
  */
 #ifndef SFFN_H
 #define SFFN_H
@@ -186,7 +185,7 @@ sffn_status sffn_decode_predicted(const void *x, const sffn_ffn_weights *w, cons
  *              [0, d_ff) is skipped and recorded as SFFN_ERR_DEVICE in the
  *              workspace's error word (sffn_read_device_error).
  *   n_core     0 <= n_core <= d_ff (0: the plain keep-ratio selection).
- * bf16 / fp32 weights (int4-g64: SFFN_ERR_UNSUPPORTED, as keep-ratio). */
+ * Every weight format (fp32, bf16, int4-g64). */
 sffn_status sffn_decode_tiered(const void *x, int B, const sffn_ffn_weights *w, int score, float keep_ratio,
                                const int32_t *core_idx, int n_core, void *out, int32_t *active_idx, int32_t *n_active,
                                void *workspace, size_t ws_bytes, sffn_stream_t stream);

@@ -173,15 +173,21 @@ def test_config_qwen_int4_threshold_full(sffn, a):
     assert abs(r["n_active"].mean() / layer["d_ff"] - a) < 0.01
 
 
-def test_int4_keep_ratio_unsupported(sffn):
-    layer = {k: (v.cuda() if torch.is_tensor(v) else v) for k, v in
-             W.make_ffn_layer(4, seed=1, d_model=512, d_ff=128).items()}
-    w = sffn.Weights(layer)
-    w.set_down_norms(sffn.down_norms(w))
-    x = W.make_tokens(4, 1, d_model=512).cuda()
-    with pytest.raises(sffn.SffnError) as e:
-        sffn.decode(x, w, sffn.MODE_KEEP_RATIO, sffn.SCORE_GATE, 0.5)
-    assert e.value.status == sffn.ERR_UNSUPPORTED
+@pytest.mark.parametrize("score", ["gate", "gate_up"])
+@pytest.mark.parametrize("B", [1, 4])
+def test_int4_keep_ratio(sffn, score, B):
+    # int4-g64 weights in the keep-ratio path: scores from the int4 gate
+    # kernel, the radix select, then the scaled int4 W_up / W_downT rows
+    layer = W.make_ffn_layer(4, seed=11, d_model=512, d_ff=1024)
+    x = W.make_tokens(4, 2 * B, seed=11, d_model=512)
+    run_and_check_decode(sffn, layer, x, "keep_ratio", score, 0.125, batch=B)
+
+
+def test_int4_keep_ratio_config_shape(sffn):
+    # the int4 workload's layer shape (d_model 2048, d_ff 11008), tier M = 4
+    layer = W.make_ffn_layer(4, seed=12)
+    x = W.make_tokens(4, 2, seed=12)
+    run_and_check_decode(sffn, layer, x, "keep_ratio", "gate_up", 0.25, batch=1, nthreads=16)
 
 
 # More neurons than (#SMs x 256): the gate kernel's chunks cannot all be resident
