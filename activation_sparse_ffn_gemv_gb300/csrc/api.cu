@@ -415,7 +415,8 @@ sffn_status sffn_prefill(const void *x, const void *y_attn, int L, const sffn_ff
     if (!x || !y_attn || !sel_idx || !n_sel || !out) return SFFN_ERR_INVALID_ARG;
     sffn_status st = check_weights(w, false);
     if (st != SFFN_OK) return st;
-    if (w->wdtype != SFFN_BF16 || w->act != SFFN_ACT_SILU || w->b_gate) return SFFN_ERR_UNSUPPORTED;
+    if ((w->wdtype != SFFN_BF16 && w->wdtype != SFFN_INT4_G64) || w->act != SFFN_ACT_SILU || w->b_gate)
+        return SFFN_ERR_UNSUPPORTED;
     if (L < 1 || L > (1 << 20) || w->d_model % 64 != 0 || w->d_ff % 128 != 0) return SFFN_ERR_SHAPE;
     if (!aligned16(x) || !aligned16(y_attn) || !aligned16(out)) return SFFN_ERR_ALIGNMENT;
     PrefillPlan p = make_prefill_plan(L, w->d_model, w->d_ff);

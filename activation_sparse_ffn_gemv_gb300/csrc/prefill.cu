@@ -19,6 +19,12 @@
 // TMA tile loads into a 4-stage shared-memory ring (128-byte swizzle), warp 1
 // owns the TMEM allocation and issues tcgen05.mma (128 x 256 x 16, fp32
 // accumulators double-buffered in TMEM), warps 2-5 drain TMEM with tcgen05.ld.
+// With int4-g64 weights (the RedKnot write-up measures INT4 Qwen3-32B) warps
+// 6-13 fill each stage's weight tile instead of TMA: a thread loads one
+// 64-code run of a stored row (32 bytes, six stages ahead) and its fp16 group
+// scale, and writes the 64 values code * scale in bf16 (see dequant_row64) as
+// one 128-byte row of the tile in the same 128-byte swizzle the MMA
+// descriptors expect (K-major for W_gate / W_up, MN-major for W_downT).
 // Tiles are rasterised in groups of m-tiles so weight tiles are reused from L2.
 // Every mbarrier wait is bounded; the selected-token count and indices are
 // read on the device and checked against L.
@@ -107,6 +113,7 @@ constexpr int G_A_BYTES = GBM * GBK * 2;         // 16 KB
 constexpr int G_B_BYTES = GMMA_N * GBK * 2;      // 32 KB
 constexpr int G_STAGE_BYTES = G_A_BYTES + G_B_BYTES;
 constexpr int kGemmThreads = 192;                // producer, MMA, 4 epilogue warps
+constexpr int kDequantThreads = 256;             // int4 weights: one 64-code run of the tile per thread
 constexpr int kTmemCols = 2 * GMMA_N;            // two accumulators of 128 x 256 fp32
 constexpr size_t kGemmSmem = (size_t)GSTAGES * G_STAGE_BYTES + 1024 /*alignment*/ + 256 /*barriers*/;
 
@@ -114,6 +121,11 @@ enum { EPI_SWIGLU = 0, EPI_DOWN = 1 };
 
 struct GemmArgs {
     const int32_t *n_sel;      // selected-token count (device)
+    // int4-g64 weights: packed codes [F, d/2] (low nibble = even column) and fp16
+    // group scales [F, d/64]; SwiGLU: W_gate (0) and W_up (1); Down: W_downT (0)
+    const uint8_t *qw0, *qw1;
+    const __half *qs0, *qs1;
+    int qd;                    // d_model
     const int32_t *sel_idx;    // EPI_DOWN: selected token ids, ascending
     const uint16_t *ysel;      // EPI_DOWN: compact residual rows [L, d]
     uint16_t *out;             // EPI_SWIGLU: H [L, d_ff]; EPI_DOWN: out [L, d]
@@ -135,8 +147,38 @@ SFFN_DEV void tile_coords(int t, int m_tiles, int n_tiles, int group_m, int &mt,
     nt = local / gm;
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// 64 int4 codes (32 bytes) times the group scale in bf16, as one 128-byte
+// tile row with its 16-byte chunks in 128-byte swizzle order.  Per pair of
+// columns (2e, 2e+1): one byte permute and one LOP3 place the two unsigned
+// nibbles (code + 8) in the mantissas of bf16 128.0, one bf16x2 fma subtracts
+// 136 (the codes, exactly), one bf16x2 multiply applies the scale s2 = (s, s)
+// (the fp16 scale rounded to bf16): two roundings to bf16, relative error at
+// most 2^-8 per weight.
+SFFN_DEV uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+SFFN_DEV void dequant_row64(const uint4 &c0, const uint4 &c1, uint32_t s2, unsigned char *dst_row, int key) {
+    const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t v = w[c] ^ 0x88888888u;  // code + 8 per nibble; column k in bits 4k
+        const uint32_t lo = v & 0x0F0F0F0Fu, hi = (v >> 4) & 0x0F0F0F0Fu;  // byte e: column 2e / 2e + 1
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t p = (__byte_perm(lo, hi, (uint32_t)(e | ((4 + e) << 8))) & 0x00FF00FFu) | 0x43004300u;
+            const uint32_t code = bf16x2_fma(p, 0x3F803F80u, 0xC308C308u);  // p * 1 - 136
+            pk[e] = bf16x2_fma(code, s2, 0x80008000u);                     // code * s + (-0)
+        }
+        *reinterpret_cast<uint4 *>(dst_row + ((c ^ key) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+}
+
+template <int EPI, bool QB>
+__global__ void __launch_bounds__(kGemmThreads + (QB ? kDequantThreads : 0), 1)
     k_gemm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b0,
            const __grid_constant__ CUtensorMap map_b1, const GemmArgs a) {
     extern __shared__ unsigned char gsm_raw[];
@@ -146,7 +188,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t *tfull = empty + GSTAGES;    // [2] accumulator ready
     uint64_t *tempty = tfull + 2;         // [2] accumulator drained
     uint64_t *mdone = tempty + 2;         // all MMAs of this CTA complete
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mdone + 1);
+    uint64_t *bready = mdone + 1;         // [GSTAGES] int4: the stage's weight tile is written
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bready + GSTAGES);
     __shared__ volatile int s_abort;
     __shared__ int s_consumed;            // k-blocks consumed by the MMA warp (for draining)
 
@@ -161,14 +204,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tempty[b], 4);
         }
         mbar_init(mdone, 1);
+        if (QB)
+            for (int s = 0; s < GSTAGES; ++s) mbar_init(&bready[s], kDequantThreads / 32);
         s_abort = 0;
         s_consumed = 0;
         mbar_fence_init();
     }
     if (warp == 0 && lane == 0) {
         tc::prefetch_tensormap(&map_a);
-        tc::prefetch_tensormap(&map_b0);
-        if (EPI == EPI_SWIGLU) tc::prefetch_tensormap(&map_b1);
+        if (!QB) {
+            tc::prefetch_tensormap(&map_b0);
+            if (EPI == EPI_SWIGLU) tc::prefetch_tensormap(&map_b1);
+        }
     }
     if (warp == 1) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
@@ -204,10 +251,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     unsigned char *st = gsm + s * G_STAGE_BYTES;
-                    mbar_arrive_expect_tx(&full[s], G_STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[s], QB ? G_A_BYTES : G_STAGE_BYTES);
                     const uint64_t pol = tc::l2_evict_last_policy();
                     tc::tma_load_2d(st, &map_a, kb * GBK, mt * GBM, &full[s], pol);
-                    if (EPI == EPI_SWIGLU) {
+                    if (QB) {
+                        // the weight tile is written by the dequantising warps
+                    } else if (EPI == EPI_SWIGLU) {
                         tc::tma_load_2d(st + G_A_BYTES, &map_b0, kb * GBK, nt * 128, &full[s], pol);
                         tc::tma_load_2d(st + G_A_BYTES + G_B_BYTES / 2, &map_b1, kb * GBK, nt * 128, &full[s], pol);
                     } else {
@@ -241,7 +290,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t dtm = tmem + (uint32_t)(b * GMMA_N);
                 for (int kb = 0; kb < a.kblocks; ++kb, ++it) {
                     const int s = it % GSTAGES, r = it / GSTAGES;
-                    if (!mbar_wait(&full[s], (uint32_t)(r & 1))) {
+                    if (!mbar_wait(&full[s], (uint32_t)(r & 1)) || (QB && !mbar_wait(&bready[s], (uint32_t)(r & 1)))) {
                         s_abort = 1;
                         record_error(a.err, SFFN_ERR_TIMEOUT);
                         break;
@@ -265,6 +314,103 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             // every MMA of this CTA has completed before teardown
             tc::mma_commit(mdone);
             mbar_wait(mdone, 0);
+        }
+    } else if (QB && warp >= 6) {
+        // ---------------- int4 weights: dequantise each stage's weight tile ----------------
+        const int u = tid - kGemmThreads;  // this thread's 64-code run of the tile
+        const int key = u & 7;             // 128-byte swizzle: chunk c lands at c ^ (row & 7)
+        // unit u of item (tile t, k-block kb): source codes, scale and tile row
+        auto src_of = [&](int t, int kb, const uint8_t *&cp, const __half *&sp, int &off) -> bool {
+            int mt, nt;
+            tile_coords(t, m_tiles, n_tiles, a.group_m, mt, nt);
+            (void)mt;
+            if (EPI == EPI_SWIGLU) {
+                const int half = u >> 7, i = u & 127, n = nt * 128 + i;
+                cp = (half ? a.qw1 : a.qw0) + (size_t)n * (a.qd / 2) + kb * 32;
+                sp = (half ? a.qs1 : a.qs0) + (size_t)n * (a.qd / 64) + kb;
+                off = half * (G_B_BYTES / 2) + i * 128;
+                return true;
+            } else {
+                const int q = u >> 6, k = u & 63, row = kb * GBK + k, col = nt * GMMA_N + q * 64;
+                off = q * (G_B_BYTES / 4) + k * 128;
+                if (col >= a.n_out) return false;  // beyond d_model: zeros
+                cp = a.qw0 + (size_t)row * (a.qd / 2) + col / 2;
+                sp = a.qs0 + (size_t)row * (a.qd / 64) + col / 64;
+                return true;
+            }
+        };
+        struct Run {
+            uint4 c0, c1;
+            uint32_t s2;  // the group scale as a bf16 pair
+            bool ok;
+        };
+        auto fetch = [&](int t, int kb) {
+            Run rn{make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), 0u, false};
+            const uint8_t *cp;
+            const __half *sp;
+            int off;
+            if (t < num_tiles && src_of(t, kb, cp, sp, off)) {
+                rn.c0 = ldg_stream(cp);
+                rn.c1 = ldg_stream(cp + 16);
+                const uint32_t sb = f32_to_bf16_bits(__half2float(__ldg(sp)));
+                rn.s2 = sb | (sb << 16);
+                rn.ok = true;
+            }
+            return rn;
+        };
+        auto advance = [&](int &t, int &kb) {
+            if (++kb == a.kblocks) {
+                kb = 0;
+                t += gridDim.x;
+            }
+        };
+        // kLook items ahead: the code loads of item it + kLook are issued when item
+        // it has been written (registers, rotated by a fully unrolled inner loop)
+        constexpr int kLook = 6;
+        Run q[kLook];
+        int t = blockIdx.x, kb = 0, tf = blockIdx.x, kbf = 0;
+#pragma unroll
+        for (int i = 0; i < kLook; ++i) {
+            q[i] = fetch(tf, kbf);
+            advance(tf, kbf);
+        }
+        bool run = true;
+        for (int it0 = 0; run; it0 += kLook) {
+#pragma unroll
+            for (int i = 0; i < kLook; ++i) {
+                if (!run) break;
+                if (t >= num_tiles || s_abort) {
+                    run = false;
+                    break;
+                }
+                const int it = it0 + i, s = it % GSTAGES, r = it / GSTAGES;
+                const bool ok = mbar_wait(&empty[s], (uint32_t)((r & 1) ^ 1));
+                if (!__all_sync(0xffffffffu, ok && !s_abort)) {
+                    if (lane == 0 && !ok) {
+                        s_abort = 1;
+                        record_error(a.err, SFFN_ERR_TIMEOUT);
+                    }
+                    run = false;
+                    break;
+                }
+                const uint8_t *cp;
+                const __half *sp;
+                int off;
+                src_of(t, kb, cp, sp, off);
+                unsigned char *dst = gsm + s * G_STAGE_BYTES + G_A_BYTES + off;
+                if (q[i].ok) {
+                    dequant_row64(q[i].c0, q[i].c1, q[i].s2, dst, key);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4 *>(dst + 16 * c) = make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();  // the tile is read by the tensor cores (async proxy)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bready[s]);
+                q[i] = fetch(tf, kbf);
+                advance(tf, kbf);
+                advance(t, kb);
+            }
         }
     } else {
         // ---------------- epilogue: warps 2..5, TMEM lane quadrant warp % 4 ----------------
@@ -414,13 +560,19 @@ sffn_status run_prefill(const void *x, const void *y_attn, int L, const sffn_ffn
     const int d = p.d, F = p.F;
     const int sms = device_sm_count();
 
+    const bool q = w->wdtype == SFFN_INT4_G64;
     CUtensorMap m_ysel, m_wg, m_wu, m_h, m_wd;
     if (!make_map(&m_ysel, ysel, (uint64_t)L, (uint64_t)d, GBK, GBM) ||
-        !make_map(&m_wg, w->w_gate, (uint64_t)F, (uint64_t)d, GBK, 128) ||
-        !make_map(&m_wu, w->w_up, (uint64_t)F, (uint64_t)d, GBK, 128) ||
-        !make_map(&m_h, h, (uint64_t)L, (uint64_t)F, GBK, GBM) ||
-        !make_map(&m_wd, w->w_downT, (uint64_t)F, (uint64_t)d, 64, GBK))
+        !make_map(&m_h, h, (uint64_t)L, (uint64_t)F, GBK, GBM))
         return SFFN_ERR_UNSUPPORTED;
+    if (q) {  // the weight tiles are dequantised in the kernel: no weight maps
+        m_wg = m_wu = m_ysel;
+        m_wd = m_h;
+    } else if (!make_map(&m_wg, w->w_gate, (uint64_t)F, (uint64_t)d, GBK, 128) ||
+               !make_map(&m_wu, w->w_up, (uint64_t)F, (uint64_t)d, GBK, 128) ||
+               !make_map(&m_wd, w->w_downT, (uint64_t)F, (uint64_t)d, 64, GBK)) {
+        return SFFN_ERR_UNSUPPORTED;
+    }
 
     long long items = 2LL * L;
     int grid = (int)((items + kResWarps - 1) / kResWarps);
@@ -439,9 +591,22 @@ sffn_status run_prefill(const void *x, const void *y_attn, int L, const sffn_ffn
     g1.kblocks = (d + GBK - 1) / GBK;
     g1.group_m = 16;
     g1.err = err;
-    e = set_max_smem((const void *)k_gemm<EPI_SWIGLU>, (int)kGemmSmem);
-    if (e == cudaSuccess)
-        e = launch_k(k_gemm<EPI_SWIGLU>, dim3(sms), dim3(kGemmThreads), kGemmSmem, s, m_ysel, m_wg, m_wu, g1);
+    g1.qw0 = static_cast<const uint8_t *>(w->w_gate);
+    g1.qw1 = static_cast<const uint8_t *>(w->w_up);
+    g1.qs0 = static_cast<const __half *>(w->s_gate);
+    g1.qs1 = static_cast<const __half *>(w->s_up);
+    g1.qd = d;
+    if (q) {
+        e = set_max_smem((const void *)k_gemm<EPI_SWIGLU, true>, (int)kGemmSmem);
+        if (e == cudaSuccess)
+            e = launch_k(k_gemm<EPI_SWIGLU, true>, dim3(sms), dim3(kGemmThreads + kDequantThreads), kGemmSmem, s,
+                         m_ysel, m_wg, m_wu, g1);
+    } else {
+        e = set_max_smem((const void *)k_gemm<EPI_SWIGLU, false>, (int)kGemmSmem);
+        if (e == cudaSuccess)
+            e = launch_k(k_gemm<EPI_SWIGLU, false>, dim3(sms), dim3(kGemmThreads), kGemmSmem, s, m_ysel, m_wg, m_wu,
+                         g1);
+    }
     if (e != cudaSuccess) return SFFN_ERR_CUDA;
 
     GemmArgs g2 = {};
@@ -455,9 +620,19 @@ sffn_status run_prefill(const void *x, const void *y_attn, int L, const sffn_ffn
     g2.kblocks = (F + GBK - 1) / GBK;
     g2.group_m = 8;
     g2.err = err;
-    e = set_max_smem((const void *)k_gemm<EPI_DOWN>, (int)kGemmSmem);
-    if (e == cudaSuccess)
-        e = launch_k(k_gemm<EPI_DOWN>, dim3(sms), dim3(kGemmThreads), kGemmSmem, s, m_h, m_wd, m_wd, g2);
+    g2.qw0 = static_cast<const uint8_t *>(w->w_downT);
+    g2.qs0 = static_cast<const __half *>(w->s_downT);
+    g2.qd = d;
+    if (q) {
+        e = set_max_smem((const void *)k_gemm<EPI_DOWN, true>, (int)kGemmSmem);
+        if (e == cudaSuccess)
+            e = launch_k(k_gemm<EPI_DOWN, true>, dim3(sms), dim3(kGemmThreads + kDequantThreads), kGemmSmem, s, m_h,
+                         m_wd, m_wd, g2);
+    } else {
+        e = set_max_smem((const void *)k_gemm<EPI_DOWN, false>, (int)kGemmSmem);
+        if (e == cudaSuccess)
+            e = launch_k(k_gemm<EPI_DOWN, false>, dim3(sms), dim3(kGemmThreads), kGemmSmem, s, m_h, m_wd, m_wd, g2);
+    }
     return e == cudaSuccess ? SFFN_OK : SFFN_ERR_CUDA;
 }
 

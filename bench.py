@@ -750,6 +750,26 @@ def bench_prefill(args, dev, rank, world, dist):
                         "frac": rows["0.5"]["ffn_frac_bf16_peak"], "peak_source": peak_src,
                         "flops_per_launch": 6.0 * rows["0.5"]["n_sel"] * d * F,
                         "traffic": traffic_for("prefill_m05")}}
+    # the same selection with int4-g64 weights (the write-up's INT4 setting)
+    layer4 = W.make_ffn_layer(4, seed=7 + rank, d_model=d, d_ff=F, device=dev)
+    w4 = sffn.Weights(layer4)
+    ws4 = sffn.alloc_workspace(sffn.WS_PREFILL, L, w4, dev)
+    torch.cuda.synchronize()
+    rows4 = {}
+    for m in (0.2, 0.5, 1.0):
+        sffn.token_select(Ya, m, c["recent_n"], c["min_keep"], sel_idx=sel, n_sel=n, workspace=ws_sel, stream=stream)
+
+        def ffn4():
+            sffn.prefill(X, Ya, w4, sel, n, out=out, workspace=ws4, stream=stream)
+        ms = _time_graph(ffn4, stream, args.prefill_steps, args.warmup)
+        k = int(n.item())
+        tf = 6.0 * k * d * F / (ms * 1e-3) / 1e12
+        rows4[str(m)] = {"n_sel": k, "ffn_ms": round(ms, 4), "ffn_tflops": round(tf, 1),
+                         "ffn_frac_bf16_peak": round(tf / bf16_peak, 4),
+                         "ffn_vs_bf16": round(rows[str(m)]["ffn_ms"] / ms, 3)}
+    res["int4_g64"] = {"workload": "the same layer shape with int4-g64 weights (codes U{-8..7}, fp16 group "
+                                   "scales), dequantised to bf16 tiles inside the GEMMs", "by_mass": rows4}
+    del layer4, w4, ws4
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = prefill_cpu_baseline(layer, X, Ya)
     return res

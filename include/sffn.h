@@ -308,8 +308,10 @@ sffn_status sffn_token_select(const void *y_attn, int L, int d_model, float mass
  * row; for the selected rows out[t] = bf16(Y[t] + FFN(Y[t])) with
  * FFN(y) = W_down . (SiLU(W_gate . y) (.) (W_up . y)); for the others
  * out[t] = Y[t] (Z = 0).  x, y_attn, out: bf16 [L, d_model].  sel_idx / n_sel as
- * written by sffn_token_select (ascending, device).  Weights: bf16, act SILU,
- * no gate bias, d_model % 64 == 0, d_ff % 128 == 0. */
+ * written by sffn_token_select (ascending, device).  Weights: bf16 or int4-g64
+ * (the INT4 setting the RedKnot write-up measures: each weight becomes
+ * code * scale rounded once to bf16 for the tensor cores), act SILU, no gate
+ * bias, d_model % 64 == 0, d_ff % 128 == 0. */
 sffn_status sffn_prefill(const void *x, const void *y_attn, int L, const sffn_ffn_weights *w,
                          const int32_t *sel_idx, const int32_t *n_sel, void *out, void *workspace,
                          size_t ws_bytes, sffn_stream_t stream);
