@@ -356,6 +356,10 @@ def bench_decode_sweeps(args, dev, T=256):
     stream = torch.cuda.Stream(device=dev)
     hbm = peaks()[0]
     out = {}
+    legs = set(args.sweep.split(",")) if getattr(args, "sweep", None) else None
+
+    def want(name):
+        return legs is None or name in legs
 
     def rowb(c):
         d = c["d_model"]
@@ -399,178 +403,183 @@ def bench_decode_sweeps(args, dev, T=256):
                 sffn.decode_dense(x[sl], ws[t % nl], out=bufs["o"][sl], workspace=bufs["work"], stream=stream)
         return _time_graph(enq, stream, max(3, args.steps // 3), args.warmup) * 1e3 / T
 
-    # ---- int4 sweep: threshold tau_a = (1 - a) quantile of the layer's gate scores
-    c = W.CONFIGS[4]
-    nl = c["layers"]
-    layers, ws, x, bufs = setup(4, nl)
-    calib = W.make_tokens(4, 256, seed=77, device=dev)
-    sc_ws = sffn.alloc_workspace(sffn.WS_DECODE, 8, ws[0], dev)
-    torch.cuda.synchronize()
-    taus = []
-    for w in ws:
-        sc = torch.cat([sffn.gate_scores(calib[i:i + 8], w, sffn.SCORE_GATE, workspace=sc_ws)
-                        for i in range(0, 256, 8)])
-        taus.append(torch.quantile(sc.flatten()[::4].float(),
-                                   torch.tensor([1.0 - a for a in c["sweep_a"]], device=dev)).tolist())
-    F, r = c["d_ff"], rowb(c)
-    dense_us = run_dense(ws, x, bufs, 1)
-    sweep = []
-    for i, a_t in enumerate(c["sweep_a"]):
-        us = run_sparse(ws, x, bufs, 1, sffn.MODE_THRESHOLD, sffn.SCORE_GATE,
-                        [taus[l][i] if a_t < 1.0 else 0.0 for l in range(nl)])
-        a = float(bufs["n"].float().mean().item()) / F
-        sweep.append(point(us, F * r * (1 + 2 * a), a_target=a_t, a=round(a, 4),
-                           speedup_vs_dense=round(dense_us / us, 3)))
-    # breakeven: where the sparse call takes as long as the dense layer, linear
-    # between swept points ("<" / ">" outside the sweep)
-    be = None
-    for p0, p1 in zip(sweep, sweep[1:]):
-        if p0["us_per_token"] <= dense_us <= p1["us_per_token"] and p1["us_per_token"] > p0["us_per_token"]:
-            be = round(p0["a"] + (dense_us - p0["us_per_token"]) * (p1["a"] - p0["a"]) /
-                       (p1["us_per_token"] - p0["us_per_token"]), 3)
-            break
-    if be is None and sweep:
-        be = f"< {sweep[0]['a']}" if sweep[0]["us_per_token"] > dense_us else (
-            f">= {sweep[-1]['a']}" if sweep[-1]["us_per_token"] <= dense_us else None)
-    out["int4_threshold_sweep"] = {
-        "workload": "qwen2.5-3b-swiglu-int4g64: d_model 2048, d_ff 11008, 36 layers, threshold on "
-                    "|SiLU(g)|*||W_down[:,j]||, B=1",
-        "dense": point(dense_us, 3 * F * r, kernel="sffn_decode_dense: every neuron, the three matrices read once"),
-        "points": sweep, "breakeven_active_fraction": be}
-    # int4 keep-ratio tiers (gate-and-up score: W_up read in full)
-    kr4 = {}
-    for M in (2, 4, 8):
-        us = run_sparse(ws, x, bufs, 1, sffn.MODE_KEEP_RATIO, sffn.SCORE_GATE_UP, [1.0 / M] * nl)
-        a = float(bufs["n"].float().mean().item()) / F
-        kr4[str(M)] = point(us, F * r * (2 + a), a=round(a, 4), speedup_vs_dense=round(dense_us / us, 3))
-    out["int4_keep_ratio"] = {"workload": "as int4_threshold_sweep, keep the top d_ff/M gate-and-up scores",
-                              "by_M": kr4}
-    del layers, ws, x, bufs, sc_ws
-    torch.cuda.empty_cache()
+    if want("int4"):
+        # ---- int4 sweep: threshold tau_a = (1 - a) quantile of the layer's gate scores
+        c = W.CONFIGS[4]
+        nl = c["layers"]
+        layers, ws, x, bufs = setup(4, nl)
+        calib = W.make_tokens(4, 256, seed=77, device=dev)
+        sc_ws = sffn.alloc_workspace(sffn.WS_DECODE, 8, ws[0], dev)
+        torch.cuda.synchronize()
+        taus = []
+        for w in ws:
+            sc = torch.cat([sffn.gate_scores(calib[i:i + 8], w, sffn.SCORE_GATE, workspace=sc_ws)
+                            for i in range(0, 256, 8)])
+            taus.append(torch.quantile(sc.flatten()[::4].float(),
+                                       torch.tensor([1.0 - a for a in c["sweep_a"]], device=dev)).tolist())
+        F, r = c["d_ff"], rowb(c)
+        dense_us = run_dense(ws, x, bufs, 1)
+        sweep = []
+        for i, a_t in enumerate(c["sweep_a"]):
+            us = run_sparse(ws, x, bufs, 1, sffn.MODE_THRESHOLD, sffn.SCORE_GATE,
+                            [taus[l][i] if a_t < 1.0 else 0.0 for l in range(nl)])
+            a = float(bufs["n"].float().mean().item()) / F
+            sweep.append(point(us, F * r * (1 + 2 * a), a_target=a_t, a=round(a, 4),
+                               speedup_vs_dense=round(dense_us / us, 3)))
+        # breakeven: where the sparse call takes as long as the dense layer, linear
+        # between swept points ("<" / ">" outside the sweep)
+        be = None
+        for p0, p1 in zip(sweep, sweep[1:]):
+            if p0["us_per_token"] <= dense_us <= p1["us_per_token"] and p1["us_per_token"] > p0["us_per_token"]:
+                be = round(p0["a"] + (dense_us - p0["us_per_token"]) * (p1["a"] - p0["a"]) /
+                           (p1["us_per_token"] - p0["us_per_token"]), 3)
+                break
+        if be is None and sweep:
+            be = f"< {sweep[0]['a']}" if sweep[0]["us_per_token"] > dense_us else (
+                f">= {sweep[-1]['a']}" if sweep[-1]["us_per_token"] <= dense_us else None)
+        out["int4_threshold_sweep"] = {
+            "workload": "qwen2.5-3b-swiglu-int4g64: d_model 2048, d_ff 11008, 36 layers, threshold on "
+                        "|SiLU(g)|*||W_down[:,j]||, B=1",
+            "dense": point(dense_us, 3 * F * r, kernel="sffn_decode_dense: every neuron, the three matrices read once"),
+            "points": sweep, "breakeven_active_fraction": be}
+        # int4 keep-ratio tiers (gate-and-up score: W_up read in full)
+        kr4 = {}
+        for M in (2, 4, 8):
+            us = run_sparse(ws, x, bufs, 1, sffn.MODE_KEEP_RATIO, sffn.SCORE_GATE_UP, [1.0 / M] * nl)
+            a = float(bufs["n"].float().mean().item()) / F
+            kr4[str(M)] = point(us, F * r * (2 + a), a=round(a, 4), speedup_vs_dense=round(dense_us / us, 3))
+        out["int4_keep_ratio"] = {"workload": "as int4_threshold_sweep, keep the top d_ff/M gate-and-up scores",
+                                  "by_M": kr4}
+        del layers, ws, x, bufs, sc_ws
+        torch.cuda.empty_cache()
 
-    # ---- Llama shape, exact gating: batched tokens (the union of the tokens'
-    # active rows is read once) and the dense layer at B = 1
-    c = W.CONFIGS[2]
-    F, r = c["d_ff"], rowb(c)
-    bt = {}
-    for B in (1, 2, 4, 8):
-        layers, ws, x, bufs = setup(2, 8, B=B, norms=False)
-        us = run_sparse(ws, x, bufs, B, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0] * 8) / B
-        n = bufs["n"].cpu().numpy()
-        idx = bufs["idx"].cpu().numpy()
-        uni = np.mean([np.unique(np.concatenate([idx[t * B + b, : n[t * B + b]] for b in range(B)])).size
-                       for t in range(T)]) / F
-        bt[str(B)] = point(us, F * r * (1 + 2 * uni) / B, a_per_token=round(float(n.mean()) / F, 4),
-                           union_fraction=round(float(uni), 4))
-        if B == 1:
-            dus = run_dense(ws, x, bufs, 1)
-            bt["dense_B1"] = point(dus, 3 * F * r, speedup_of_sparse_B1=round(dus / us, 3))
+    if want("batch"):
+        # ---- Llama shape, exact gating: batched tokens (the union of the tokens'
+        # active rows is read once) and the dense layer at B = 1
+        c = W.CONFIGS[2]
+        F, r = c["d_ff"], rowb(c)
+        bt = {}
+        for B in (1, 2, 4, 8):
+            layers, ws, x, bufs = setup(2, 8, B=B, norms=False)
+            us = run_sparse(ws, x, bufs, B, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0] * 8) / B
+            n = bufs["n"].cpu().numpy()
+            idx = bufs["idx"].cpu().numpy()
+            uni = np.mean([np.unique(np.concatenate([idx[t * B + b, : n[t * B + b]] for b in range(B)])).size
+                           for t in range(T)]) / F
+            bt[str(B)] = point(us, F * r * (1 + 2 * uni) / B, a_per_token=round(float(n.mean()) / F, 4),
+                               union_fraction=round(float(uni), 4))
+            if B == 1:
+                dus = run_dense(ws, x, bufs, 1)
+                bt["dense_B1"] = point(dus, 3 * F * r, speedup_of_sparse_B1=round(dus / us, 3))
+            del layers, ws, x, bufs
+            torch.cuda.empty_cache()
+        out["llama_exact_by_batch"] = bt
+
+    if want("keep_ratio"):
+        # ---- keep-ratio tiers: the gate-and-up score (W_up read in full, only W_down
+        # sparse) and the gate score (W_up and W_down sparse)
+        c = W.CONFIGS[3]
+        F, r = c["d_ff"], rowb(c)
+        layers, ws, x, bufs = setup(3, c["layers"])
+        kr = {}
+        for name, score in (("gate_up", sffn.SCORE_GATE_UP), ("gate", sffn.SCORE_GATE)):
+            by = {}
+            for M in c["keep_M"]:
+                us = run_sparse(ws, x, bufs, 1, sffn.MODE_KEEP_RATIO, score, [1.0 / M] * c["layers"])
+                a = float(bufs["n"].float().mean().item()) / F
+                by[str(M)] = point(us, F * r * ((2 + a) if score == sffn.SCORE_GATE_UP else (1 + 2 * a)), a=round(a, 4))
+            kr[name] = by
+        out["keep_ratio"] = {"workload": "qwen2.5-3b-swiglu: d_model 2048, d_ff 11008 bf16, 36 layers, keep the "
+                                         "top d_ff/M scores, B=1", "by_score": kr}
+
+        # ---- tier tables (sffn_decode_tiered): per layer a core of half the tier
+        # from 64 calibration tokens (sffn_tier_core_set), the rest chosen online
+        xc = W.make_tokens(3, 64, seed=99, device=dev)
+        tiers = {}
+        for name, score in (("gate_up", sffn.SCORE_GATE_UP), ("gate", sffn.SCORE_GATE)):
+            by = {}
+            for M in (4, 8):
+                k = max(1, int(F / M))
+                t0 = torch.cuda.Event(enable_timing=True)
+                t1 = torch.cuda.Event(enable_timing=True)
+                cores = []
+                for l, w in enumerate(ws):
+                    sc = torch.cat([sffn.gate_scores(xc[i:i + 8], w, score) for i in range(0, 64, 8)])
+                    if l == 0:
+                        t0.record()
+                    cores.append(sffn.tier_core_set(sc, k, k // 2))
+                    if l == 0:
+                        t1.record()
+                torch.cuda.synchronize()
+
+                def enq():
+                    for t in range(T):
+                        sffn.decode_tiered(x[t:t + 1], ws[t % c["layers"]], score, 1.0 / M, cores[t % c["layers"]],
+                                           out=bufs["o"][t:t + 1], active_idx=bufs["idx"][t:t + 1],
+                                           n_active=bufs["n"][t:t + 1], workspace=bufs["work"], stream=stream)
+                us = _time_graph(enq, stream, max(3, args.steps // 3), args.warmup) * 1e3 / T
+                a = float(bufs["n"][:T].float().mean().item()) / F
+                nb = F * r * ((2 + a) if score == sffn.SCORE_GATE_UP else (1 + 2 * a))
+                by[str(M)] = point(us, nb, a=round(a, 4), core=k // 2,
+                                   speedup_vs_keep_ratio=round(kr[name][str(M)]["us_per_token"] / us, 3),
+                                   core_set_ms=round(t0.elapsed_time(t1), 4))
+            tiers[name] = by
+        out["tiered"] = {"workload": "as keep_ratio, with a per-layer core of k/2 columns from 64 calibration tokens; "
+                                     "core_set_ms: sffn_tier_core_set for one layer (offline)", "by_score": tiers}
         del layers, ws, x, bufs
         torch.cuda.empty_cache()
-    out["llama_exact_by_batch"] = bt
 
-    # ---- keep-ratio tiers: the gate-and-up score (W_up read in full, only W_down
-    # sparse) and the gate score (W_up and W_down sparse)
-    c = W.CONFIGS[3]
-    F, r = c["d_ff"], rowb(c)
-    layers, ws, x, bufs = setup(3, c["layers"])
-    kr = {}
-    for name, score in (("gate_up", sffn.SCORE_GATE_UP), ("gate", sffn.SCORE_GATE)):
-        by = {}
-        for M in c["keep_M"]:
-            us = run_sparse(ws, x, bufs, 1, sffn.MODE_KEEP_RATIO, score, [1.0 / M] * c["layers"])
-            a = float(bufs["n"].float().mean().item()) / F
-            by[str(M)] = point(us, F * r * ((2 + a) if score == sffn.SCORE_GATE_UP else (1 + 2 * a)), a=round(a, 4))
-        kr[name] = by
-    out["keep_ratio"] = {"workload": "qwen2.5-3b-swiglu: d_model 2048, d_ff 11008 bf16, 36 layers, keep the "
-                                     "top d_ff/M scores, B=1", "by_score": kr}
-
-    # ---- tier tables (sffn_decode_tiered): per layer a core of half the tier
-    # from 64 calibration tokens (sffn_tier_core_set), the rest chosen online
-    xc = W.make_tokens(3, 64, seed=99, device=dev)
-    tiers = {}
-    for name, score in (("gate_up", sffn.SCORE_GATE_UP), ("gate", sffn.SCORE_GATE)):
-        by = {}
-        for M in (4, 8):
-            k = max(1, int(F / M))
-            t0 = torch.cuda.Event(enable_timing=True)
-            t1 = torch.cuda.Event(enable_timing=True)
-            cores = []
-            for l, w in enumerate(ws):
-                sc = torch.cat([sffn.gate_scores(xc[i:i + 8], w, score) for i in range(0, 64, 8)])
-                if l == 0:
-                    t0.record()
-                cores.append(sffn.tier_core_set(sc, k, k // 2))
-                if l == 0:
-                    t1.record()
-            torch.cuda.synchronize()
+    if want("predictor"):
+        # ---- low-rank gate predictor on the Llama shape (sffn_decode_predicted):
+        # random rank-256 fp32 factors (timing only: quality needs trained weights),
+        # A scaled so that A (B x) spreads like the gate bias; alpha per layer so a
+        # target share of the timed tokens' neurons are candidates
+        c = W.CONFIGS[2]
+        F, d, nl, rank = c["d_ff"], c["d_model"], c["layers"], 256
+        layers, ws, x, bufs = setup(2, nl, norms=False)
+        gen = torch.Generator(device=dev).manual_seed(11)
+        xt = x[:T].float()
+        facs, preds = [], []
+        for l in range(nl):
+            A = torch.randn(F, rank, generator=gen, device=dev) / rank ** 0.5
+            Bf = torch.randn(rank, d, generator=gen, device=dev) / d ** 0.5
+            q = (xt @ Bf.t()) @ A.t()
+            A = (A * (0.5 / q.std())).contiguous()
+            bias = layers[l]["b_gate"].to(dev).float()
+            facs.append((A, Bf.contiguous()))
+            preds.append((xt @ Bf.t()) @ A.t() + bias[None, :])
+        exact_us = run_sparse(ws, x, bufs, 1, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0] * nl)
+        lr = {"workload": "llama2-7b-reglu shape (d_model 4096, d_ff 11008 bf16, 8 layers), B=1, rank-256 fp32 "
+                          "factors (random: timing only), exact rule on the candidates",
+              "exact_decode_us_per_token": round(exact_us, 3), "points": []}
+        for frac in (0.15, 0.3, 0.5):
+            alphas, cand = [], []
+            for l in range(nl):
+                v = torch.quantile(preds[l][l::nl].flatten(), 1.0 - frac).item()
+                alphas.append(max(0.0, -v))
+                cand.append((preds[l][l::nl] >= -alphas[-1]).float().mean().item())
 
             def enq():
                 for t in range(T):
-                    sffn.decode_tiered(x[t:t + 1], ws[t % c["layers"]], score, 1.0 / M, cores[t % c["layers"]],
-                                       out=bufs["o"][t:t + 1], active_idx=bufs["idx"][t:t + 1],
-                                       n_active=bufs["n"][t:t + 1], workspace=bufs["work"], stream=stream)
+                    A, Bf = facs[t % nl]
+                    sffn.decode_predicted(x[t:t + 1], ws[t % nl], A, Bf, alphas[t % nl], out=bufs["o"][t:t + 1],
+                                          active_idx=bufs["idx"][t:t + 1], n_active=bufs["n"][t:t + 1],
+                                          workspace=bufs["work"], stream=stream)
             us = _time_graph(enq, stream, max(3, args.steps // 3), args.warmup) * 1e3 / T
             a = float(bufs["n"][:T].float().mean().item()) / F
-            nb = F * r * ((2 + a) if score == sffn.SCORE_GATE_UP else (1 + 2 * a))
-            by[str(M)] = point(us, nb, a=round(a, 4), core=k // 2,
-                               speedup_vs_keep_ratio=round(kr[name][str(M)]["us_per_token"] / us, 3),
-                               core_set_ms=round(t0.elapsed_time(t1), 4))
-        tiers[name] = by
-    out["tiered"] = {"workload": "as keep_ratio, with a per-layer core of k/2 columns from 64 calibration tokens; "
-                                 "core_set_ms: sffn_tier_core_set for one layer (offline)", "by_score": tiers}
-    del layers, ws, x, bufs
-    torch.cuda.empty_cache()
+            cf = sum(cand) / nl
+            nbytes = 4.0 * rank * (F + d) + rowb(c) * F * (cf + 2 * a)
+            lr["points"].append(point(us, nbytes, candidates=round(cf, 4), a=round(a, 4),
+                                      speedup_vs_exact=round(exact_us / us, 3)))
+        out["lowrank_predictor"] = lr
+        del layers, ws, x, bufs, facs, preds
+        torch.cuda.empty_cache()
 
-    # ---- low-rank gate predictor on the Llama shape (sffn_decode_predicted):
-    # random rank-256 fp32 factors (timing only: quality needs trained weights),
-    # A scaled so that A (B x) spreads like the gate bias; alpha per layer so a
-    # target share of the timed tokens' neurons are candidates
-    c = W.CONFIGS[2]
-    F, d, nl, rank = c["d_ff"], c["d_model"], c["layers"], 256
-    layers, ws, x, bufs = setup(2, nl, norms=False)
-    gen = torch.Generator(device=dev).manual_seed(11)
-    xt = x[:T].float()
-    facs, preds = [], []
-    for l in range(nl):
-        A = torch.randn(F, rank, generator=gen, device=dev) / rank ** 0.5
-        Bf = torch.randn(rank, d, generator=gen, device=dev) / d ** 0.5
-        q = (xt @ Bf.t()) @ A.t()
-        A = (A * (0.5 / q.std())).contiguous()
-        bias = layers[l]["b_gate"].to(dev).float()
-        facs.append((A, Bf.contiguous()))
-        preds.append((xt @ Bf.t()) @ A.t() + bias[None, :])
-    exact_us = run_sparse(ws, x, bufs, 1, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0] * nl)
-    lr = {"workload": "llama2-7b-reglu shape (d_model 4096, d_ff 11008 bf16, 8 layers), B=1, rank-256 fp32 "
-                      "factors (random: timing only), exact rule on the candidates",
-          "exact_decode_us_per_token": round(exact_us, 3), "points": []}
-    for frac in (0.15, 0.3, 0.5):
-        alphas, cand = [], []
-        for l in range(nl):
-            v = torch.quantile(preds[l][l::nl].flatten(), 1.0 - frac).item()
-            alphas.append(max(0.0, -v))
-            cand.append((preds[l][l::nl] >= -alphas[-1]).float().mean().item())
-
-        def enq():
-            for t in range(T):
-                A, Bf = facs[t % nl]
-                sffn.decode_predicted(x[t:t + 1], ws[t % nl], A, Bf, alphas[t % nl], out=bufs["o"][t:t + 1],
-                                      active_idx=bufs["idx"][t:t + 1], n_active=bufs["n"][t:t + 1],
-                                      workspace=bufs["work"], stream=stream)
-        us = _time_graph(enq, stream, max(3, args.steps // 3), args.warmup) * 1e3 / T
-        a = float(bufs["n"][:T].float().mean().item()) / F
-        cf = sum(cand) / nl
-        nbytes = 4.0 * rank * (F + d) + rowb(c) * F * (cf + 2 * a)
-        lr["points"].append(point(us, nbytes, candidates=round(cf, 4), a=round(a, 4),
-                                  speedup_vs_exact=round(exact_us / us, 3)))
-    out["lowrank_predictor"] = lr
-    del layers, ws, x, bufs, facs, preds
-    torch.cuda.empty_cache()
-
-    # ---- tiny fp32 ReGLU layer (L2 resident, launch bound: us/token only)
-    layers, ws, x, bufs = setup(1, 1, norms=False)
-    us = run_sparse(ws, x, bufs, 1, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0])
-    out["tiny_fp32"] = {"us_per_token": round(us, 3), "a": round(float(bufs["n"].float().mean().item()) / 688, 4)}
+    if want("tiny"):
+        # ---- tiny fp32 ReGLU layer (L2 resident, launch bound: us/token only)
+        layers, ws, x, bufs = setup(1, 1, norms=False)
+        us = run_sparse(ws, x, bufs, 1, sffn.MODE_EXACT, sffn.SCORE_GATE, [0.0])
+        out["tiny_fp32"] = {"us_per_token": round(us, 3), "a": round(float(bufs["n"].float().mean().item()) / 688, 4)}
     return out
 
 
@@ -860,6 +869,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-sweeps", action="store_true")
+    ap.add_argument("--sweep", default=None,
+                    help="comma-separated decode workload legs to run (int4, batch, keep_ratio, predictor, tiny); "
+                         "default all")
     ap.add_argument("--no-decode", action="store_true", help="run only the prefill leg (profiling)")
     ap.add_argument("--prefill-steps", type=int, default=10)
     args = ap.parse_args()
