@@ -587,30 +587,36 @@ __global__ void __launch_bounds__(kSelThreads) k_keep_ratio(KeepArgs a) {
     TopkChunk ch = topk_chunk(key, F, forced, cut, tmp);
 
     const bool want_h = a.lh && a.nb == 1;  // h_j = a_j * u_j for the selected neurons
+    // a_j outside the selection is read only through the union of B > 1 tokens
+    const bool zero_rest = a.nb > 1;
     float *aeff = a.aeff + (size_t)b * F;
     int32_t *lidx = a.lidx + (size_t)b * F;
-    constexpr int U = 4;  // mask words per step: the a_j, u_j loads of a step are issued together
+    constexpr int U = 4;  // mask words per step: their selections first, then the a_j, u_j loads together
     for (int w = ch.w0; w < ch.w1; w += U) {
+        TopkWord t[U];
+#pragma unroll
+        for (int q = 0; q < U; ++q) {
+            t[q] = TopkWord{false, 0, 0u};
+            if (w + q < ch.w1) t[q] = topk_word(key, F, forced, cut, w + q, ch);
+        }
         float av[U], uv[U];
 #pragma unroll
         for (int q = 0; q < U; ++q) {
             const int j = 32 * (w + q) + lane;
-            const bool ld = want_h && w + q < ch.w1 && j < F;
-            av[q] = ld ? aeff[j] : 0.f;
-            uv[q] = ld ? a.uval[j] : 0.f;
+            av[q] = want_h && t[q].sel ? aeff[j] : 0.f;
+            uv[q] = want_h && t[q].sel ? a.uval[j] : 0.f;
         }
 #pragma unroll
         for (int q = 0; q < U; ++q) {
             if (w + q >= ch.w1) break;
             const int j = 32 * (w + q) + lane;
-            const TopkWord t = topk_word(key, F, forced, cut, w + q, ch);
-            if (t.sel) {
-                if (want_h) a.lh[t.pos] = av[q] * uv[q];
-                lidx[t.pos] = j;
-            } else if (j < F) {
+            if (t[q].sel) {
+                if (want_h) a.lh[t[q].pos] = av[q] * uv[q];
+                lidx[t[q].pos] = j;
+            } else if (zero_rest && j < F) {
                 aeff[j] = 0.f;
             }
-            if (lane == 0 && a.mask) a.mask[(size_t)b * nwords + w + q] = t.bal;
+            if (lane == 0 && a.mask) a.mask[(size_t)b * nwords + w + q] = t[q].bal;
         }
     }
     for (int c = tid; c < a.C; c += blockDim.x) a.cnt[(size_t)b * a.C + c] = c == 0 ? ch.total : 0;

@@ -38,17 +38,19 @@ SFFN_DEV int find_cross_bin(const unsigned *hist, int nbins, unsigned need, unsi
     return bin;
 }
 
-// Copy n 32-bit keys into shared memory (eight loads in flight per thread).
+// Copy n 32-bit keys into shared memory (sixteen loads in flight per thread:
+// one memory round trip up to 16 x blockDim keys).
 SFFN_DEV void stage_keys(uint32_t *dst, const uint32_t *src, int n) {
-    for (int j0 = threadIdx.x; j0 < n; j0 += 8 * blockDim.x) {
-        uint32_t v[8];
+    constexpr int K = 16;
+    for (int j0 = threadIdx.x; j0 < n; j0 += K * blockDim.x) {
+        uint32_t v[K];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < K; ++k) {
             const int j = j0 + k * blockDim.x;
-            v[k] = j < n ? src[j] : 0u;
+            v[k] = j < n ? __ldcg(src + j) : 0u;
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < K; ++k) {
             const int j = j0 + k * blockDim.x;
             if (j < n) dst[j] = v[k];
         }
