@@ -12,7 +12,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libsffn.so")
-SOURCES = ["api.cu", "decode.cu", "decode_tc.cu", "select.cu", "prefill.cu", "noalloc.cu", "schedule.cu", "predict.cu", "tiers.cu", "moe.cu"]
+SOURCES = ["api.cu", "decode.cu", "decode_tc.cu", "decode_q1.cu", "select.cu", "prefill.cu", "noalloc.cu", "schedule.cu", "predict.cu", "tiers.cu", "moe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

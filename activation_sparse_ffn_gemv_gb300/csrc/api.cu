@@ -216,9 +216,6 @@ sffn_status sffn_decode_dense(const void *x, int B, const sffn_ffn_weights *w, v
     if (w->wdtype != SFFN_BF16 && w->wdtype != SFFN_INT4_G64) return SFFN_ERR_UNSUPPORTED;
     if (device_sm_count() <= 0) return SFFN_ERR_CUDA;
     DecodePlan p = make_decode_plan(B, w->d_model, w->d_ff);
-    if (!decode_tc_shape_ok(w, p)) return SFFN_ERR_UNSUPPORTED;
-    st = check_ws(workspace, ws_bytes, p.total);
-    if (st != SFFN_OK) return st;
     DecodeCall c = {};
     c.x = x;
     c.w = w;
@@ -226,7 +223,11 @@ sffn_status sffn_decode_dense(const void *x, int B, const sffn_ffn_weights *w, v
     c.mode = SFFN_MODE_EXACT;
     c.out = out;
     c.ws = workspace;
-    st = run_decode_tc(c, p, (cudaStream_t)stream, true);
+    const bool q1 = decode_q1_eligible(c, p, true);
+    if (!q1 && !decode_tc_shape_ok(w, p)) return SFFN_ERR_UNSUPPORTED;
+    st = check_ws(workspace, ws_bytes, p.total);
+    if (st != SFFN_OK) return st;
+    st = q1 ? run_decode_q1(c, p, (cudaStream_t)stream, true) : run_decode_tc(c, p, (cudaStream_t)stream, true);
     if (st == SFFN_OK) st = cuda_status(cudaGetLastError());
     return st;
 }

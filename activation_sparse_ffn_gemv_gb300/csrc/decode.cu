@@ -1331,6 +1331,7 @@ sffn_status run_reduce_chunks(const DecodeCall &c, const DecodePlan &p, cudaStre
 }
 
 sffn_status run_decode(const DecodeCall &c, const DecodePlan &p, cudaStream_t s) {
+    if (decode_q1_eligible(c, p, false)) return run_decode_q1(c, p, s, false);
     if (decode_tc_eligible(c, p)) return run_decode_tc(c, p, s, false);
     cudaError_t e;
     switch (c.w->wdtype) {

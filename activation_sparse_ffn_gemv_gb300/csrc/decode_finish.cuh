@@ -30,32 +30,42 @@ struct FinishArgs {
 // gbar[0] counts arrivals and is never reset; this call's barrier opens once it
 // has grown by gridDim.x past the base (unsigned differences, so wrap-around is
 // harmless).
+// Release add / acquire load of a grid-barrier counter at GPU scope.
+SFFN_DEV void red_release_add(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+SFFN_DEV unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 SFFN_DEV void finish_call(const FinishArgs &a, unsigned bar_base, bool failed) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t total = (size_t)a.nb * a.d;
     const int NR = (int)min((size_t)gridDim.x, max((total + 31) / 32, (size_t)(gridDim.x + 3) / 4));
     __shared__ int s_bar_ok;
     __shared__ float red[8][32];
-    __threadfence();
+    // The arrival is one release add at GPU scope after a CTA barrier: every
+    // write of the CTA (partials, counts, lists) happens before it.  A reducer
+    // polls with acquire loads and passes the result on through a CTA barrier.
     __syncthreads();
     if ((int)blockIdx.x >= NR) {
-        if (tid == 0) atomicAdd(a.gbar, 1u);
+        if (tid == 0) red_release_add(a.gbar, 1u);
         return;
     }
     if (tid == 0) {
-        atomicAdd(a.gbar, 1u);
-        const volatile unsigned *arrivals = a.gbar;
+        red_release_add(a.gbar, 1u);
         int ok = 1;
-        if (*arrivals - bar_base < gridDim.x) {
+        if (ld_acquire(a.gbar) - bar_base < gridDim.x) {
             const uint64_t t0 = globaltimer_ns();
-            while (*arrivals - bar_base < gridDim.x)
+            while (ld_acquire(a.gbar) - bar_base < gridDim.x)
                 if (globaltimer_ns() - t0 > kWaitLimitNs) {
                     ok = 0;
                     record_error(a.err, SFFN_ERR_TIMEOUT);
                     break;
                 }
         }
-        __threadfence();
         s_bar_ok = ok;
     }
     __syncthreads();

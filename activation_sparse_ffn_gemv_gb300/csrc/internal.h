@@ -89,6 +89,9 @@ sffn_status run_decode(const DecodeCall &c, const DecodePlan &p, cudaStream_t s)
 bool decode_tc_shape_ok(const sffn_ffn_weights *w, const DecodePlan &p);
 bool decode_tc_eligible(const DecodeCall &c, const DecodePlan &p);
 sffn_status run_decode_tc(const DecodeCall &c, const DecodePlan &p, cudaStream_t s, bool dense);
+// One-token int4 decode on the CUDA cores (decode_q1.cu); dense = every neuron.
+bool decode_q1_eligible(const DecodeCall &c, const DecodePlan &p, bool dense);
+sffn_status run_decode_q1(const DecodeCall &c, const DecodePlan &p, cudaStream_t s, bool dense);
 sffn_status run_down_norms(const sffn_ffn_weights *w, float *norms, cudaStream_t s);
 // One-token finish over per-chunk partials and lists in the workspace (part
 // [C, d], cnt [C], lidx [C, R]): the fixed-order reduction and the list writes.

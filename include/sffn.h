@@ -40,7 +40,10 @@
  *  - Calls are asynchronous and stream-ordered on `stream` (NULL = the legacy
  *    default stream); nothing is read back to the host, so a sequence of calls
  *    can be captured in a CUDA graph.  Counts (n_active, n_sel) stay on the
- *    device.  Consecutive kernels use programmatic dependent launch.
+ *    device.  Consecutive kernels use programmatic dependent launch; a decode
+ *    call's kernel starts reading its weight matrices, scales and gate bias
+ *    before it waits for the preceding kernel of this library on the stream
+ *    (no call of this library writes them).
  *  - Argument errors are detected on the host before anything is launched and
  *    returned as a status; a failed launch returns SFFN_ERR_CUDA.  Contract
  *    violations that only the device can see (an out-of-range selected-token
@@ -141,8 +144,9 @@ sffn_status sffn_decode(const void *x, int B, const sffn_ffn_weights *w, int mod
  * layer against (breakeven active fraction, speedup at 10% active).  Reads all
  * three matrices once; no index lists.  x, out: bf16 [B, d_model]; weights bf16
  * or int4-g64; workspace as sffn_decode's (sffn_workspace_size(0, B, w)).
- * Needs d_model % 512 == 0, d_model <= 4096 and d_ff <= 128 * (#SMs); other
- * shapes and fp32 weights return SFFN_ERR_UNSUPPORTED. */
+ * Needs d_model in {1024, 2048, 4096} and d_ff <= 128 * (#SMs); a single
+ * token with int4-g64 weights also takes d_model 512 and d_ff up to
+ * 256 * (#SMs).  Other shapes and fp32 weights return SFFN_ERR_UNSUPPORTED. */
 sffn_status sffn_decode_dense(const void *x, int B, const sffn_ffn_weights *w, void *out, void *workspace,
                               size_t ws_bytes, sffn_stream_t stream);
 

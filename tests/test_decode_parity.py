@@ -259,6 +259,23 @@ def test_config_llama_reglu_batched(sffn, B):
     assert abs(r["n_active"].mean() / layer["d_ff"] - 0.125) < 0.02
 
 
+@pytest.mark.parametrize("d,F,mode", [(1024, 1500, "exact"), (4096, 2900, "threshold"), (512, 37, "threshold"),
+                                      (2048, 40, "exact"), (4096, 11008, "exact")])
+def test_int4_single_token_shapes(sffn, d, F, mode):
+    # one token with int4 weights at each supported d_model: ReLU + bias for
+    # exact gating, SiLU with a threshold at the 0.7 quantile; ragged chunks
+    act = "relu" if mode == "exact" else "silu"
+    layer = W.make_ffn_layer(4, seed=41 + d + F, d_model=d, d_ff=F, act=act)
+    if mode == "exact":
+        layer["b_gate"] = torch.full((F,), -0.05)
+    x = W.make_tokens(4, 1, seed=41 + F, d_model=d)
+    if mode == "exact":
+        r = run_and_check_decode(sffn, layer, x, "exact")
+    else:
+        r = run_and_check_decode(sffn, layer, x, "threshold", "gate", _tau_at(layer, x, 0.7))
+    assert 0 < r["n_active"][0] < F
+
+
 def test_int4_exact_relu_small_chunks(sffn):
     # int4 weights with ReLU gating and a bias; ragged last tile of each chunk
     d, F = 1024, 1500
@@ -272,6 +289,8 @@ def test_int4_exact_relu_small_chunks(sffn):
 DENSE = [
     # (cfg, d, F, wdtype, act, B)
     (4, 2048, 11008, "int4_g64", "silu", 1),
+    (4, 4096, 3000, "int4_g64", "silu", 1),
+    (4, 512, 333, "int4_g64", "relu", 1),
     (4, 1024, 700, "int4_g64", "silu", 3),
     (2, 4096, 11008, "bf16", "relu", 1),
     (3, 1024, 2050, "bf16", "silu", 8),
