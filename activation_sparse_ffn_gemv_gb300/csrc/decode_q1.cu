@@ -185,6 +185,54 @@ SFFN_DEV void split_word(uint32_t w, uint32_t &lo, uint32_t &hi) {
     hi = ((w >> 4) & 0x0F0F0F0Fu) ^ 0x08080808u;
 }
 
+// x fragments of the GPW groups from group g0 on, in the order the codes are
+// unpacked: per 32-column block bb and quad lane q, columns 32 bb + 8 q +
+// {0,4 | 1,5} and {2,6 | 3,7}.
+template <int GPW>
+SFFN_DEV void q1_x_frags(uint32_t (&bx)[GPW][8], const uint16_t *x, int g0, int q) {
+#pragma unroll
+    for (int i = 0; i < GPW; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int bb = 2 * (g0 + i) + h;
+            const uint4 v = ldg_v4(x + 32 * bb + 8 * q);
+            bx[i][4 * h + 0] = __byte_perm(v.x, v.z, 0x5410);
+            bx[i][4 * h + 1] = __byte_perm(v.x, v.z, 0x7632);
+            bx[i][4 * h + 2] = __byte_perm(v.y, v.w, 0x5410);
+            bx[i][4 * h + 3] = __byte_perm(v.y, v.w, 0x7632);
+        }
+    }
+}
+
+// Row sums over the GPW groups from g0 of one 16-row tile: rows at base + i *
+// stride (i clamped below n), group scales at sbase + i * sstride.  The sums
+// of rows tile * 16 + (0..15) go to out[0..15] (lanes with q == 0 store).
+template <int GPW>
+SFFN_DEV void q1_tile_dots(const unsigned char *base, uint32_t stride, const unsigned char *sbase, uint32_t sstride,
+                           int tile, int n, int g0, const uint32_t (&bx)[GPW][8], float *out) {
+    const int lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lblk = lane >> 4;  // ldmatrix row / 16-byte block
+    const int ri = min(kQ1Tile * tile + lrow, n - 1);
+    const uint32_t rowaddr = smem_u32(base + (size_t)ri * stride) + 16u * lblk;
+    const int r0i = min(kQ1Tile * tile + g, n - 1), r1i = min(kQ1Tile * tile + g + 8, n - 1);
+    const unsigned char *s0 = sbase + (size_t)r0i * sstride, *s1 = sbase + (size_t)r1i * sstride;
+    uint32_t w[GPW][4];
+#pragma unroll
+    for (int i = 0; i < GPW; ++i) q1_ldsm4(rowaddr + 32u * (g0 + i), w[i][0], w[i][1], w[i][2], w[i][3]);
+    float dd[GPW][4];
+    q1_groups<GPW>(dd, w, bx);
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < GPW; ++i) {
+        acc0 = fmaf(dd[i][0], __half2float(*reinterpret_cast<const __half *>(s0 + 2 * (g0 + i))), acc0);
+        acc1 = fmaf(dd[i][2], __half2float(*reinterpret_cast<const __half *>(s1 + 2 * (g0 + i))), acc1);
+    }
+    if (q == 0) {
+        out[g] = acc0;
+        out[g + 8] = acc1;
+    }
+}
+
 template <int CS, bool DENSE>
 __global__ void __launch_bounds__(kQ1Threads, q1_ctas_per_sm(CS)) k_gate_q1(Q1Args a) {
     constexpr int D = 256 * CS;                   // d_model
@@ -213,7 +261,7 @@ __global__ void __launch_bounds__(kQ1Threads, q1_ctas_per_sm(CS)) k_gate_q1(Q1Ar
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wc = warp;
-    const int g = lane >> 2, q = lane & 3;        // MMA fragment coordinates
+    const int q = lane & 3;                        // quad lane of the MMA fragments
     const int F = a.F, R = a.R;
     const int row0 = blockIdx.x * R, nrows = min(R, F - row0);
     const int ntiles = (nrows + kQ1Tile - 1) / kQ1Tile;
@@ -257,50 +305,12 @@ __global__ void __launch_bounds__(kQ1Threads, q1_ctas_per_sm(CS)) k_gate_q1(Q1Ar
     // the rows' ||W_down[:, j]|| (threshold rule; they may come from the previous kernel)
     if (tid < nrows) snorm[tid] = !DENSE && a.mode == SFFN_MODE_THRESHOLD ? a.norms[row0 + tid] : 0.f;
 
-    // x fragments of this warp's groups, in the order the codes are unpacked:
-    // per 32-column block bb and quad lane q, columns 32 bb + 8 q + {0,4 | 1,5}
-    // and {2,6 | 3,7}
     uint32_t bx[GPW][8];
-#pragma unroll
-    for (int i = 0; i < GPW; ++i) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int bb = 2 * (wc * GPW + i) + h;
-            const uint4 v = ldg_v4(a.x + 32 * bb + 8 * q);
-            bx[i][4 * h + 0] = __byte_perm(v.x, v.z, 0x5410);
-            bx[i][4 * h + 1] = __byte_perm(v.x, v.z, 0x7632);
-            bx[i][4 * h + 2] = __byte_perm(v.y, v.w, 0x5410);
-            bx[i][4 * h + 3] = __byte_perm(v.y, v.w, 0x7632);
-        }
-    }
-    // this lane's ldmatrix row within a tile and 16-byte block within a group
-    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lblk = lane >> 4;
+    q1_x_frags<GPW>(bx, a.x, wc * GPW, q);
     bool ok = true;
-
-    // row sums of 16-row tiles: rows at base + i * stride (i clamped below n),
-    // group scales at sbase + i * sstride; partial of this warp's groups to red
     auto tile_dots = [&](const unsigned char *base, uint32_t stride, const unsigned char *sbase, uint32_t sstride,
                          int tile, int n) {
-        const int ri = min(kQ1Tile * tile + lrow, n - 1);
-        const uint32_t rowaddr = smem_u32(base + (size_t)ri * stride) + 16u * lblk;
-        const int r0i = min(kQ1Tile * tile + g, n - 1), r1i = min(kQ1Tile * tile + g + 8, n - 1);
-        const unsigned char *s0 = sbase + (size_t)r0i * sstride, *s1 = sbase + (size_t)r1i * sstride;
-        uint32_t w[GPW][4];
-#pragma unroll
-        for (int i = 0; i < GPW; ++i) q1_ldsm4(rowaddr + 32u * (wc * GPW + i), w[i][0], w[i][1], w[i][2], w[i][3]);
-        float dd[GPW][4];
-        q1_groups<GPW>(dd, w, bx);
-        float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < GPW; ++i) {
-            const int grp = wc * GPW + i;
-            acc0 = fmaf(dd[i][0], __half2float(*reinterpret_cast<const __half *>(s0 + 2 * grp)), acc0);
-            acc1 = fmaf(dd[i][2], __half2float(*reinterpret_cast<const __half *>(s1 + 2 * grp)), acc1);
-        }
-        if (q == 0) {
-            red[wc * kQ1MaxRows + kQ1Tile * tile + g] = acc0;
-            red[wc * kQ1MaxRows + kQ1Tile * tile + g + 8] = acc1;
-        }
+        q1_tile_dots<GPW>(base, stride, sbase, sstride, tile, n, wc * GPW, bx, red + wc * kQ1MaxRows + kQ1Tile * tile);
     };
 
     // ---- gate
@@ -469,6 +479,210 @@ __global__ void __launch_bounds__(kQ1Threads, q1_ctas_per_sm(CS)) k_gate_q1(Q1Ar
     finish_call(fa, bar_base, failed);
 }
 
+
+// ---------------------------------------------------------------------------
+// The dense layer (every neuron) as one stream.  Every row is used, so nothing
+// waits for a decision: tiles of 16 rows of W_gate, W_up and W_downT (with
+// their scales) flow through a ring of shared-memory stages by bulk copies,
+// the first stages before the wait for the previous kernel.  Warps 0-7 take the
+// gate and warps 8-15 the up dot products of a tile (the MMA contraction of the
+// gate kernel, each warp a share of the 64-column groups); 16 threads form
+// h_j = act(g_j + b_j) u_j; then every thread adds (scale h_j) * code of the
+// tile's down rows into its 8 output columns (rows in ascending order within a
+// thread group, the groups added in order at the end).
+constexpr int kQ1DThreads = 512;
+constexpr int kQ1DWarps = kQ1DThreads / 32;
+constexpr int kQ1DMaxStages = 8;
+
+// Bytes of one stage: 16 gate and 16 up rows at the padded stride, 16 down
+// rows, the three matrices' scales.
+SFFN_HOST_DEV constexpr uint32_t q1d_stage_bytes(int cs) {
+    return 2u * kQ1Tile * q1_gate_stride(cs) + kQ1Tile * q1_row_bytes(cs) + 3u * kQ1Tile * q1_scale_bytes(cs);
+}
+
+template <int CS>
+__global__ void __launch_bounds__(kQ1DThreads, 1) k_dense_q1(Q1Args a, int nstages) {
+    constexpr int D = 256 * CS;
+    constexpr uint32_t RB = q1_row_bytes(CS);
+    constexpr uint32_t SB = q1_scale_bytes(CS);
+    constexpr uint32_t PS = q1_gate_stride(CS);
+    constexpr uint32_t ST = q1d_stage_bytes(CS);
+    constexpr uint32_t OFF_U = kQ1Tile * PS, OFF_D = 2 * kQ1Tile * PS, OFF_GS = OFF_D + kQ1Tile * RB;
+    constexpr uint32_t OFF_US = OFF_GS + kQ1Tile * SB, OFF_DS = OFF_US + kQ1Tile * SB;
+    constexpr int GPW = 4 * CS / 8;               // 64-column groups per warp (8 warps per matrix)
+    constexpr int TPR = D / 8;                    // down: threads per row (8 columns each)
+    constexpr int DG = kQ1DThreads / TPR;         // down: thread groups
+    static_assert(DG * TPR == kQ1DThreads, "down thread groups");
+    extern __shared__ __align__(128) unsigned char sm[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm);           // [kQ1DMaxStages]
+    unsigned char *stages = sm + 128;
+    __shared__ float sbias[kQ1MaxRows];
+    __shared__ float red[2][2][8][kQ1Tile];  // [tile parity][gate, up][warp][row]
+    __shared__ int s_fail;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int mat = warp >> 3, wc = warp & 7;     // 0: gate, 1: up
+    const int F = a.F, R = a.R;
+    const int row0 = blockIdx.x * R, nrows = min(R, F - row0);
+    const int ntiles = (nrows + kQ1Tile - 1) / kQ1Tile;
+    const int NS = nstages;
+    const uint64_t pol = l2_evict_first_policy();
+
+    // tile tt into its stage (warp 0)
+    auto issue_tile = [&](int tt) {
+        unsigned char *st = stages + (size_t)(tt % NS) * ST;
+        uint64_t *bar = &full[tt % NS];
+        const int r0 = kQ1Tile * tt, nr = min(kQ1Tile, nrows - r0);
+        const size_t j0 = (size_t)(row0 + r0);
+        fence_proxy_async_smem();
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nr * (3u * RB + 3u * SB));
+        __syncwarp();
+        if (lane < nr) bulk_load(st + (size_t)lane * PS, a.wg + (j0 + lane) * RB, RB, bar, pol);
+        else if (lane >= kQ1Tile && lane - kQ1Tile < nr)
+            bulk_load(st + OFF_U + (size_t)(lane - kQ1Tile) * PS, a.wu + (j0 + lane - kQ1Tile) * RB, RB, bar, pol);
+        if (lane == 0) bulk_load(st + OFF_D, a.wd + j0 * RB, (uint32_t)nr * RB, bar, pol);
+        if (lane == 1) bulk_load(st + OFF_GS, a.sg + j0 * (SB / 2), (uint32_t)nr * SB, bar, pol);
+        if (lane == 2) bulk_load(st + OFF_US, a.su + j0 * (SB / 2), (uint32_t)nr * SB, bar, pol);
+        if (lane == 3) bulk_load(st + OFF_DS, a.sd + j0 * (SB / 2), (uint32_t)nr * SB, bar, pol);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+        mbar_fence_init();
+        s_fail = 0;
+    }
+    if (tid < nrows) sbias[tid] = a.bias ? __ldg(a.bias + row0 + tid) : 0.f;
+    __syncthreads();
+    // weights are inputs of the call: the first stages stream before the wait
+    if (warp == 0)
+        for (int tt = 0; tt < min(NS, ntiles); ++tt) issue_tile(tt);
+
+    griddep_wait();
+    griddep_launch_dependents();
+    const unsigned bar_base = *reinterpret_cast<volatile unsigned *>(a.gbar + 1);
+
+    uint32_t bx[GPW][8];
+    q1_x_frags<GPW>(bx, a.x, wc * GPW, lane & 3);
+    const int dg = tid / TPR, tg = tid - dg * TPR, col0 = 8 * tg;
+    float2 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[k] = make_float2(0.f, 0.f);
+    bool ok = true;
+
+    for (int t = 0; t < ntiles; ++t) {
+        const unsigned char *st = stages + (size_t)(t % NS) * ST;
+        ok &= mbar_wait(&full[t % NS], (uint32_t)((t / NS) & 1));
+        const int nr = min(kQ1Tile, nrows - kQ1Tile * t);
+        // gate (warps 0-7) or up (warps 8-15) sums of the tile's rows
+        q1_tile_dots<GPW>(st + (mat ? OFF_U : 0u), PS, st + (mat ? OFF_US : OFF_GS), SB, 0, nr, wc * GPW, bx,
+                          red[t & 1][mat][wc]);
+        // the sums are in; every thread is done with tile t - 1's stage and with
+        // the sums of tile t - 1 (the other half of red, written next by tile t + 1)
+        __syncthreads();
+        if (warp == 0 && t > 0 && t - 1 + NS < ntiles) issue_tile(t - 1 + NS);
+        // every warp forms the tile's h_j (lane j), so no second barrier
+        float hj = 0.f;
+        if (lane < nr) {
+            float gs = 0.f, us = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                gs += red[t & 1][0][c][lane];
+                us += red[t & 1][1][c][lane];
+            }
+            hj = act_fn(a.act, gs + sbias[kQ1Tile * t + lane]) * us;
+        }
+        // down rows of the tile, ascending within each thread group
+#pragma unroll
+        for (int k0 = 0; k0 < kQ1Tile; k0 += DG) {
+            const int i = k0 + dg;
+            const float h = __shfl_sync(0xffffffffu, hj, i & 31);
+            if (i < nr) {
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(st + OFF_D + (size_t)i * RB + 4 * tg);
+                const float sh =
+                    __half2float(*reinterpret_cast<const __half *>(st + OFF_DS + (size_t)i * SB + (col0 >> 6) * 2)) * h;
+                const float2 s2 = make_float2(sh, sh);
+                uint32_t lo, hi;
+                split_word(w, lo, hi);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[k] = __ffma2_rn(code_pair(lo, hi, k), s2, acc[k]);
+            }
+        }
+    }
+    if (!ok) s_fail = 1;
+    __syncthreads();
+    // groups 1.. hand their sums to group 0, which adds them in group order
+    // (the stage area holds (DG - 1) d floats: q1d_smem_bytes)
+    if (DG > 1) {
+        float2 *gred = reinterpret_cast<float2 *>(stages);
+        if (dg > 0)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) gred[(size_t)(dg - 1) * (D / 2) + col0 / 2 + k] = acc[k];
+        __syncthreads();
+        if (dg == 0)
+            for (int u = 1; u < DG; ++u)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float2 v = gred[(size_t)(u - 1) * (D / 2) + col0 / 2 + k];
+                    acc[k].x += v.x;
+                    acc[k].y += v.y;
+                }
+    }
+    if (dg == 0) {
+        float4 *dst = reinterpret_cast<float4 *>(a.part + (size_t)blockIdx.x * D + col0);
+        dst[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+        dst[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+    }
+    const bool failed = s_fail != 0;
+    if (failed && tid == 0) {
+        // a wait gave up: record it and let this CTA's copies land (bounded)
+        record_error(a.err, SFFN_ERR_TIMEOUT);
+        for (int t = max(0, ntiles - NS); t < ntiles; ++t) mbar_wait(&full[t % NS], (uint32_t)((t / NS) & 1));
+    }
+
+    FinishArgs fa;
+    fa.gbar = a.gbar;
+    fa.part = a.part;
+    fa.nb = 1;
+    fa.d = D;
+    fa.F = F;
+    fa.C = a.C;
+    fa.R = R;
+    fa.cnt = nullptr;
+    fa.lidx = a.lidx;
+    fa.out = a.out;
+    fa.out_f32 = 0;
+    fa.active_idx = a.active_idx;
+    fa.n_active = a.n_active;
+    fa.err = a.err;
+    finish_call(fa, bar_base, failed);
+}
+
+// Stages of the dense stream that fit the shared memory of one CTA (0: it
+// does not fit twice).
+int q1d_stages(int cs, int R) {
+    const size_t avail = (size_t)device_smem_optin() - 128 - 4096;  // barriers; static shared memory
+    const int ntiles = (R + kQ1Tile - 1) / kQ1Tile;
+    int ns = (int)(avail / q1d_stage_bytes(cs));
+    ns = std::min(std::min(ns, kQ1DMaxStages), ntiles);
+    return ns >= 2 || (ns == 1 && ntiles == 1) ? ns : 0;
+}
+
+// Shared memory of the dense stream: barriers, then the stages, which must
+// also hold the down sums of thread groups 1.. at the end ((DG - 1) d floats,
+// DG = 4096 / d).
+size_t q1d_smem_bytes(int cs, int ns) {
+    const size_t d = 256u * (size_t)cs;
+    return 128 + std::max((size_t)ns * q1d_stage_bytes(cs), 4u * (4096u - d));
+}
+
+template <int CS>
+cudaError_t launch_q1d(const Q1Args &qa, int C, int ns, cudaStream_t s) {
+    const size_t smem = q1d_smem_bytes(CS, ns);
+    cudaError_t e = set_max_smem((const void *)k_dense_q1<CS>, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_k(k_dense_q1<CS>, dim3(C), dim3(kQ1DThreads), smem, s, qa, ns);
+}
+
 template <int CS, bool DENSE>
 cudaError_t launch_q1(const Q1Args &qa, int C, cudaStream_t s) {
     const size_t smem = q1_smem_bytes(CS, qa.R);
@@ -526,6 +740,17 @@ sffn_status run_decode_q1(const DecodeCall &c, const DecodePlan &p, cudaStream_t
     qa.n_active = c.n_active;
     qa.err = reinterpret_cast<int32_t *>(ws + p.off_err);
     cudaError_t e;
+    const int ns = dense ? q1d_stages(cs, p.R) : 0;
+    if (ns > 0) {
+        switch (cs) {
+        case 2: e = launch_q1d<2>(qa, p.C, ns, s); break;
+        case 4: e = launch_q1d<4>(qa, p.C, ns, s); break;
+        case 8: e = launch_q1d<8>(qa, p.C, ns, s); break;
+        case 16: e = launch_q1d<16>(qa, p.C, ns, s); break;
+        default: return SFFN_ERR_UNSUPPORTED;
+        }
+        return e == cudaSuccess ? SFFN_OK : SFFN_ERR_CUDA;
+    }
     switch (cs) {
     case 2: e = launch_q1_d<2>(qa, p.C, dense, s); break;
     case 4: e = launch_q1_d<4>(qa, p.C, dense, s); break;
