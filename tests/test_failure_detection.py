@@ -36,30 +36,44 @@ def _bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy()
 
 
-def test_decode_barrier_timeout_is_reported_and_recovers(S):
-    layer = layer_to(W.make_ffn_layer(2, seed=51, d_model=512, d_ff=2048), "cuda")
+# (config, weights): bf16 runs the streaming gate kernel; int4 with one token runs
+# the staged single-token kernel, and its dense layer the int4 stream kernel
+TIMEOUT_CASES = {"bf16": (2, "exact"), "int4": (4, "exact"), "int4_dense": (4, "dense")}
+
+
+@pytest.mark.parametrize("case", list(TIMEOUT_CASES))
+def test_decode_barrier_timeout_is_reported_and_recovers(S, case):
+    cfg, kind = TIMEOUT_CASES[case]
+    layer = layer_to(W.make_ffn_layer(cfg, seed=51, d_model=512, d_ff=2048), "cuda")
     w = S.Weights(layer)
-    x = W.make_tokens(2, 1, seed=51, d_model=512).cuda()
+    x = W.make_tokens(cfg, 1, seed=51, d_model=512).cuda()
     ws = S.alloc_workspace(S.WS_DECODE, 1, w)
     ctl = ws[:16].view(torch.int32)   # error word, barrier arrivals, arrivals before the call
-    ref, ref_idx, ref_n = S.decode(x, w, S.MODE_EXACT, workspace=ws)
+
+    def call():
+        if kind == "dense":
+            return S.decode_dense(x, w, workspace=ws), None, None
+        return S.decode(x, w, S.MODE_EXACT, workspace=ws)
+
+    ref, ref_idx, ref_n = call()
     torch.cuda.synchronize()
     assert S.read_device_error(ws) == 0
-    ref, ref_idx, ref_n = S.decode(x, w, S.MODE_EXACT, workspace=ws)
+    ref, ref_idx, ref_n = call()
     torch.cuda.synchronize()
     arrivals = int(ctl[1].item())
     assert arrivals > 0 and int(ctl[2].item()) == arrivals  # the pair a finished call leaves
     # a base one past the arrivals: this call's CTAs can never all be counted
     ctl[2] = arrivals + 1
     torch.cuda.synchronize()
-    S.decode(x, w, S.MODE_EXACT, workspace=ws)
+    call()
     torch.cuda.synchronize()
     assert S.read_device_error(ws) == S.ERR_TIMEOUT
     assert int(ctl.abs().sum().item()) == 0  # reading the error reset the control block
-    out, idx, n = S.decode(x, w, S.MODE_EXACT, workspace=ws)
+    out, idx, n = call()
     torch.cuda.synchronize()
     assert S.read_device_error(ws) == 0
-    assert torch.equal(n, ref_n) and torch.equal(idx[0, : int(n[0])], ref_idx[0, : int(n[0])])
+    if n is not None:
+        assert torch.equal(n, ref_n) and torch.equal(idx[0, : int(n[0])], ref_idx[0, : int(n[0])])
     assert np.array_equal(_bits(out), _bits(ref))
 
 
