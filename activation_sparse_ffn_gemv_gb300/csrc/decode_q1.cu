@@ -26,7 +26,9 @@
 //          their exact sum is multiplied by the row's fp16 group scale.  The
 //          warps split the columns (whole groups); their per-row partials are
 //          added in a fixed order.  Bias, act, score and the decision.
-//   list   The chunk's ascending list of active neurons (ballots).
+//   list   Thread j decides row j; ballots rank the active rows into the
+//          chunk's ascending list, and an active row of the first batch starts
+//          its own copies at once.
 //   batch  Each active row's W_up and W_downT rows with their scales go by bulk
 //          copies into one slot of a double-buffered batch (the next batch in
 //          flight while one is used).  u_j = W_up[j] . x as in the gate,
@@ -178,6 +180,11 @@ SFFN_DEV float2 code_pair(uint32_t lo, uint32_t hi, int k) {
     return __fadd2_rn(make_float2(a, b), make_float2(-kQ1Magic, -kQ1Magic));
 }
 
+// Raise the transaction count an mbarrier phase waits for (no arrival).
+SFFN_DEV void q1_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
 // Split a word of 8 codes (two's-complement nibbles, column k at bits 4k) into
 // the byte vectors of code + 8 for columns 0, 2, 4, 6 and 1, 3, 5, 7.
 SFFN_DEV void split_word(uint32_t w, uint32_t &lo, uint32_t &hi) {
@@ -252,12 +259,11 @@ __global__ void __launch_bounds__(kQ1Threads, q1_ctas_per_sm(CS)) k_gate_q1(Q1Ar
     uint64_t *bbar = pbar + kQ1MaxTiles;                          // [2] batch buffers
     float *red = reinterpret_cast<float *>(sm + kQ1BarBytes);     // [NWC][kQ1MaxRows]
     unsigned char *region = sm + kQ1BarBytes + sizeof(float) * NWC * kQ1MaxRows;
-    __shared__ float gact[kQ1MaxRows];
     __shared__ float sbias[kQ1MaxRows], snorm[kQ1MaxRows];
-    __shared__ uint8_t gflag[kQ1MaxRows];
     __shared__ int alist[kQ1MaxRows];
     __shared__ float hval[kQ1MaxRows];
-    __shared__ int s_n, s_fail;
+    __shared__ int wcnt[kQ1Warps];
+    __shared__ int s_fail;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int wc = warp;
@@ -321,67 +327,67 @@ __global__ void __launch_bounds__(kQ1Threads, q1_ctas_per_sm(CS)) k_gate_q1(Q1Ar
     }
     if (!ok) s_fail = 1;
     __syncthreads();
+
+    // ---- decision, the chunk's ascending list and the first batch's copies in
+    // one pass: thread tid decides row tid, ranks it by ballots, and an active
+    // row among the first `cap` starts its own W_up / W_downT copies at once
+    bool on = false;
+    float av = 0.f;
     if (tid < nrows) {
         float gs = 0.f;
 #pragma unroll
         for (int c = 0; c < NWC; ++c) gs += red[c * kQ1MaxRows + tid];
-        const float av = act_fn(a.act, gs + sbias[tid]);
-        bool on;
+        av = act_fn(a.act, gs + sbias[tid]);
         if (DENSE) on = true;
         else if (a.mode == SFFN_MODE_EXACT) on = av != 0.f;
         else on = fabsf(av) * snorm[tid] >= a.tau;
-        gact[tid] = av;
-        gflag[tid] = on ? 1 : 0;
     }
+    const unsigned bal = __ballot_sync(0xffffffffu, on);
+    if (lane == 0) wcnt[warp] = __popc(bal);
     __syncthreads();
-
-    // ---- the chunk's ascending list
-    if (warp == 0) {
-        const unsigned lt = (1u << lane) - 1u;
-        int n = 0;
-        for (int b0 = 0; b0 < nrows; b0 += 32) {
-            const int lr = b0 + lane;
-            const bool on = lr < nrows && gflag[lr];
-            const unsigned bal = __ballot_sync(0xffffffffu, on);
-            if (on) {
-                const int m = n + __popc(bal & lt);
-                alist[m] = row0 + lr;
-                hval[m] = gact[lr];
-                if (!DENSE) a.lidx[(size_t)row0 + m] = row0 + lr;
-            }
-            n += __popc(bal);
-        }
-        if (lane == 0) {
-            s_n = n;
-            if (!DENSE) a.cnt[blockIdx.x] = n;
-        }
+    int nact = 0, before = 0;
+#pragma unroll
+    for (int w = 0; w < kQ1Warps; ++w) {
+        before += w < warp ? wcnt[w] : 0;
+        nact += wcnt[w];
     }
-    __syncthreads();
-    const int nact = s_n;
     const int nbat = (nact + cap - 1) / cap;
+    // one active row's W_up and W_downT rows with their scales into slot i % cap
+    // of buffer (i / cap) & 1
+    auto issue_row = [&](int i, int64_t row, uint64_t *bar) {
+        const size_t j = (size_t)row;
+        unsigned char *sl = region + (size_t)((i / cap) & 1) * cap * SLOT + (size_t)(i % cap) * SLOT;
+        bulk_load(sl, a.wu + j * RB, RB, bar, pol);
+        bulk_load(sl + RB, a.su + j * (SB / 2), SB, bar, pol);
+        bulk_load(sl + RB + SB, a.wd + j * RB, RB, bar, pol);
+        bulk_load(sl + 2 * RB + SB, a.sd + j * (SB / 2), SB, bar, pol);
+    };
+    if (on) {
+        const int m = before + __popc(bal & ((1u << lane) - 1u));
+        alist[m] = row0 + tid;
+        hval[m] = av;
+        if (!DENSE) a.lidx[(size_t)row0 + m] = row0 + tid;
+        if (m < cap) {
+            fence_proxy_async_smem();  // every warp's reads of the gate rows passed the barrier
+            q1_expect_tx(&bbar[0], 2u * (RB + SB));
+            issue_row(m, row0 + tid, &bbar[0]);
+        }
+    }
+    if (tid == 0 && !DENSE) a.cnt[blockIdx.x] = nact;
+    __syncthreads();  // the list is complete; batch 0's transaction count is raised
+    if (tid == 0 && nact > 0) mbar_arrive(&bbar[0]);
 
-    // one batch of active rows into buffer bt & 1 (warp 0; the buffer's earlier
-    // readers have passed a barrier)
+    // batch bt >= 1 into buffer bt & 1 (warp 0; the buffer's earlier readers
+    // have passed a barrier)
     auto issue_batch = [&](int bt) {
         const int i0 = bt * cap, nb = min(cap, nact - i0);
-        unsigned char *buf = region + (size_t)(bt & 1) * cap * SLOT;
         uint64_t *bar = &bbar[bt & 1];
         fence_proxy_async_smem();
         if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nb * 2u * (RB + SB));
         __syncwarp();
-        for (int i = lane; i < nb; i += 32) {
-            const size_t j = (size_t)alist[i0 + i];
-            unsigned char *s = buf + (size_t)i * SLOT;
-            bulk_load(s, a.wu + j * RB, RB, bar, pol);
-            bulk_load(s + RB, a.su + j * (SB / 2), SB, bar, pol);
-            bulk_load(s + RB + SB, a.wd + j * RB, RB, bar, pol);
-            bulk_load(s + 2 * RB + SB, a.sd + j * (SB / 2), SB, bar, pol);
-        }
+        for (int i = lane; i < nb; i += 32) issue_row(i0 + i, alist[i0 + i], bar);
     };
-    if (warp == 0) {
-        if (nbat > 0) issue_batch(0);
-        if (nbat > 1) issue_batch(1);
-    }
+    if (warp == 0 && nbat > 1) issue_batch(1);
 
     // down: thread group dg = tid / TPR owns batch rows dg, dg + DG, ...; thread
     // tg of a group owns the 8 WPT columns from col0 (one scale group)
@@ -491,7 +497,6 @@ __global__ void __launch_bounds__(kQ1Threads, q1_ctas_per_sm(CS)) k_gate_q1(Q1Ar
 // tile's down rows into its 8 output columns (rows in ascending order within a
 // thread group, the groups added in order at the end).
 constexpr int kQ1DThreads = 512;
-constexpr int kQ1DWarps = kQ1DThreads / 32;
 constexpr int kQ1DMaxStages = 8;
 
 // Bytes of one stage: 16 gate and 16 up rows at the padded stride, 16 down
