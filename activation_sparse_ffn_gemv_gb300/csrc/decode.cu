@@ -421,7 +421,12 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
 
     // ordered compaction of this chunk: one list per token for the active_idx
     // output, and (in shared memory) the chunk's rows active for any token
-    // (row r = tid; R <= 256: one ballot per warp and list, one pass)
+    // (row r = tid; R <= 256: one ballot per warp and list, one pass).  A row
+    // of the union that falls in the first batch starts the bulk copy of its
+    // W_downT row (sent to L2 at the decision) into its ring slot right away.
+    const int cap = (int)((size_t)kGateWarps * D * stage_bytes / rspace);
+    const char *wd = static_cast<const char *>(a.wdT);
+    const char *sd = static_cast<const char *>(a.sd);
     __shared__ int sdown[kMaxChunk];
     __shared__ int s_ndown;
     __shared__ int wcnt[NB + 1][kGateWarps];
@@ -445,8 +450,22 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
             }
             const int pos = base + __popc(bl & lt);
             if (bit) {
-                if (l < a.nb) a.lidx[(size_t)l * F + row0 + pos] = row0 + tid;
-                else sdown[pos] = tid;
+                if (l < a.nb) {
+                    a.lidx[(size_t)l * F + row0 + pos] = row0 + tid;
+                } else {
+                    sdown[pos] = tid;
+                    if (pos < cap && !failed) {
+                        const size_t j = (size_t)(row0 + tid);
+                        unsigned char *dslot = ring + (size_t)pos * rspace;
+                        const uint64_t dpol = l2_evict_first_policy();
+                        fence_proxy_async_smem();  // the ring's reads passed the barrier above
+                        asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(dbar)),
+                                     "r"(rspace)
+                                     : "memory");
+                        bulk_load(dslot, wd + j * row_bytes, row_bytes, dbar, dpol);
+                        if (W::Q) bulk_load(dslot + row_bytes, sd + j * sbytes, sbytes, dbar, dpol);
+                    }
+                }
             }
             if (tid == 0) {
                 if (l < a.nb) a.cnt[(size_t)l * a.C + blockIdx.x] = tot;
@@ -462,13 +481,12 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
     // and accumulates h_j * W_down[:, j] over the rows in ascending order
     // (deterministic) into this CTA's partial.
     const int ndown = failed ? 0 : s_ndown;
-    const int cap = (int)((size_t)kGateWarps * D * stage_bytes / rspace);
-    const char *wd = static_cast<const char *>(a.wdT);
-    const char *sd = static_cast<const char *>(a.sd);
     for (int b0 = 0, batch = 0;; b0 += cap, ++batch) {
         const int bn = min(cap, ndown - b0);
         if (bn > 0) {
-            if (tid == 0) {
+            if (tid == 0 && batch == 0) {
+                mbar_arrive(dbar);  // the rows raised the count and started their copies
+            } else if (tid == 0) {
                 fence_proxy_async_smem();  // earlier generic reads of the ring precede the copies
                 const uint64_t pol = l2_evict_first_policy();
                 mbar_arrive_expect_tx(dbar, (uint32_t)bn * rspace);
