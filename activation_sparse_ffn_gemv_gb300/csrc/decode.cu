@@ -1199,7 +1199,11 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     ga.sg = w->s_gate;
     ga.su = w->s_up;
     ga.sd = w->s_downT;
-    cudaError_t e = up ? launch_gate<W, NB, true>(ga, p, s) : launch_gate<W, NB, false>(ga, p, s);
+    cudaError_t e;
+    if (W::Q && up && !ga.decide && scores_q1_eligible(w, p))  // int4, one token, gate-and-up scores
+        e = run_scores_q1(w, c.x, p, ga.score, ga.aeff, ga.uval, s);
+    else
+        e = up ? launch_gate<W, NB, true>(ga, p, s) : launch_gate<W, NB, false>(ga, p, s);
     if (e != cudaSuccess || scores_only || fused) return e;
 
     int nparts = p.G2;

@@ -662,6 +662,128 @@ __global__ void __launch_bounds__(kQ1DThreads, 1) k_dense_q1(Q1Args a, int nstag
     finish_call(fa, bar_base, failed);
 }
 
+// ---------------------------------------------------------------------------
+// Gate-and-up scores of one token for the keep-ratio rule (WiSparse write-up,
+// sec. 2.1: s_j = |a_j u_j| ||W_down[:, j]||): the same stream as the dense
+// layer without W_downT.  Tiles of 16 W_gate and W_up rows with their scales
+// flow through a ring of bulk-copied stages; warps 0-7 take the gate and 8-15
+// the up contraction; 16 threads write s_j, a_j and u_j of the tile's rows.
+SFFN_HOST_DEV constexpr uint32_t q1s_stage_bytes(int cs) {
+    return 2u * kQ1Tile * q1_gate_stride(cs) + 2u * kQ1Tile * q1_scale_bytes(cs);
+}
+
+struct Q1ScoreArgs {
+    const uint8_t *wg, *wu;
+    const __half *sg, *su;
+    const float *bias, *norms;
+    const uint16_t *x;
+    int F, R, act;
+    float *score, *aeff, *uval;   // [F] each; aeff / uval may be null
+};
+
+template <int CS>
+__global__ void __launch_bounds__(kQ1DThreads, 1) k_scores_q1(Q1ScoreArgs a, int nstages) {
+    constexpr uint32_t RB = q1_row_bytes(CS);
+    constexpr uint32_t SB = q1_scale_bytes(CS);
+    constexpr uint32_t PS = q1_gate_stride(CS);
+    constexpr uint32_t ST = q1s_stage_bytes(CS);
+    constexpr uint32_t OFF_U = kQ1Tile * PS, OFF_GS = 2 * kQ1Tile * PS, OFF_US = OFF_GS + kQ1Tile * SB;
+    constexpr int GPW = 4 * CS / 8;
+    extern __shared__ __align__(128) unsigned char sm[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(sm);
+    unsigned char *stages = sm + 128;
+    __shared__ float sbias[kQ1MaxRows], snorm[kQ1MaxRows];
+    __shared__ float red[2][2][8][kQ1Tile];
+    __shared__ int s_fail;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int mat = warp >> 3, wc = warp & 7;
+    const int F = a.F, R = a.R;
+    const int row0 = blockIdx.x * R, nrows = min(R, F - row0);
+    const int ntiles = (nrows + kQ1Tile - 1) / kQ1Tile;
+    const int NS = nstages;
+    const uint64_t pol = l2_evict_first_policy();
+
+    auto issue_tile = [&](int tt) {
+        unsigned char *st = stages + (size_t)(tt % NS) * ST;
+        uint64_t *bar = &full[tt % NS];
+        const int r0 = kQ1Tile * tt, nr = min(kQ1Tile, nrows - r0);
+        const size_t j0 = (size_t)(row0 + r0);
+        fence_proxy_async_smem();
+        if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)nr * (2u * RB + 2u * SB));
+        __syncwarp();
+        if (lane < nr) bulk_load(st + (size_t)lane * PS, a.wg + (j0 + lane) * RB, RB, bar, pol);
+        else if (lane >= kQ1Tile && lane - kQ1Tile < nr)
+            bulk_load(st + OFF_U + (size_t)(lane - kQ1Tile) * PS, a.wu + (j0 + lane - kQ1Tile) * RB, RB, bar, pol);
+        if (lane == 1) bulk_load(st + OFF_GS, a.sg + j0 * (SB / 2), (uint32_t)nr * SB, bar, pol);
+        if (lane == 2) bulk_load(st + OFF_US, a.su + j0 * (SB / 2), (uint32_t)nr * SB, bar, pol);
+    };
+
+    if (tid == 0) {
+        for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+        mbar_fence_init();
+        s_fail = 0;
+    }
+    if (tid < nrows) sbias[tid] = a.bias ? __ldg(a.bias + row0 + tid) : 0.f;
+    __syncthreads();
+    if (warp == 0)
+        for (int tt = 0; tt < min(NS, ntiles); ++tt) issue_tile(tt);
+
+    griddep_wait();
+    griddep_launch_dependents();
+    // the norms may come from the previous kernel
+    if (tid < nrows) snorm[tid] = a.norms ? a.norms[row0 + tid] : 0.f;
+    uint32_t bx[GPW][8];
+    q1_x_frags<GPW>(bx, a.x, wc * GPW, lane & 3);
+    __syncthreads();
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+        const unsigned char *st = stages + (size_t)(t % NS) * ST;
+        ok &= mbar_wait(&full[t % NS], (uint32_t)((t / NS) & 1));
+        const int nr = min(kQ1Tile, nrows - kQ1Tile * t);
+        q1_tile_dots<GPW>(st + (mat ? OFF_U : 0u), PS, st + (mat ? OFF_US : OFF_GS), SB, 0, nr, wc * GPW, bx,
+                          red[t & 1][mat][wc]);
+        // the sums are in; every thread is done with tile t - 1's stage and sums
+        __syncthreads();
+        if (warp == 0 && t > 0 && t - 1 + NS < ntiles) issue_tile(t - 1 + NS);
+        if (tid < nr) {
+            float gs = 0.f, us = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                gs += red[t & 1][0][c][tid];
+                us += red[t & 1][1][c][tid];
+            }
+            const int r = kQ1Tile * t + tid;
+            const float av = act_fn(a.act, gs + sbias[r]);
+            const size_t j = (size_t)(row0 + r);
+            a.score[j] = fabsf(av * us) * snorm[r];
+            if (a.aeff) a.aeff[j] = av;
+            if (a.uval) a.uval[j] = us;
+        }
+    }
+    if (!ok) s_fail = 1;
+    __syncthreads();
+    if (s_fail && tid == 0) {
+        // a wait gave up: let this CTA's copies land (bounded); the scores are not valid
+        for (int t = max(0, ntiles - NS); t < ntiles; ++t) mbar_wait(&full[t % NS], (uint32_t)((t / NS) & 1));
+    }
+}
+
+int q1s_stages(int cs, int R) {
+    const size_t avail = (size_t)device_smem_optin() - 128 - 6144;  // barriers; static shared memory
+    const int ntiles = (R + kQ1Tile - 1) / kQ1Tile;
+    int ns = (int)(avail / q1s_stage_bytes(cs));
+    ns = std::min(std::min(ns, kQ1DMaxStages), ntiles);
+    return ns >= 2 || (ns == 1 && ntiles == 1) ? ns : 0;
+}
+
+template <int CS>
+cudaError_t launch_q1s(const Q1ScoreArgs &sa, int C, int ns, cudaStream_t s) {
+    const size_t smem = 128 + (size_t)ns * q1s_stage_bytes(CS);
+    cudaError_t e = set_max_smem((const void *)k_scores_q1<CS>, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_k(k_scores_q1<CS>, dim3(C), dim3(kQ1DThreads), smem, s, sa, ns);
+}
+
 // Stages of the dense stream that fit the shared memory of one CTA (0: it
 // does not fit twice).
 int q1d_stages(int cs, int R) {
@@ -704,6 +826,38 @@ cudaError_t launch_q1_d(const Q1Args &qa, int C, bool dense, cudaStream_t s) {
 int q1_slices(int d) { return d == 512 ? 2 : d == 1024 ? 4 : d == 2048 ? 8 : d == 4096 ? 16 : 0; }
 
 }  // namespace
+
+bool scores_q1_eligible(const sffn_ffn_weights *w, const DecodePlan &p) {
+    if (w->wdtype != SFFN_INT4_G64 || p.nb != 1) return false;
+    const int cs = q1_slices(w->d_model);
+    return cs != 0 && p.R <= kQ1MaxRows && q1s_stages(cs, p.R) > 0;
+}
+
+cudaError_t run_scores_q1(const sffn_ffn_weights *w, const void *x, const DecodePlan &p, float *score, float *aeff,
+                          float *uval, cudaStream_t s) {
+    Q1ScoreArgs sa = {};
+    sa.wg = static_cast<const uint8_t *>(w->w_gate);
+    sa.wu = static_cast<const uint8_t *>(w->w_up);
+    sa.sg = static_cast<const __half *>(w->s_gate);
+    sa.su = static_cast<const __half *>(w->s_up);
+    sa.bias = w->b_gate;
+    sa.norms = w->down_norms;
+    sa.x = static_cast<const uint16_t *>(x);
+    sa.F = p.F;
+    sa.R = p.R;
+    sa.act = w->act;
+    sa.score = score;
+    sa.aeff = aeff;
+    sa.uval = uval;
+    const int cs = q1_slices(p.d), ns = q1s_stages(cs, p.R);
+    switch (cs) {
+    case 2: return launch_q1s<2>(sa, p.C, ns, s);
+    case 4: return launch_q1s<4>(sa, p.C, ns, s);
+    case 8: return launch_q1s<8>(sa, p.C, ns, s);
+    case 16: return launch_q1s<16>(sa, p.C, ns, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
 
 bool decode_q1_eligible(const DecodeCall &c, const DecodePlan &p, bool dense) {
     const sffn_ffn_weights *w = c.w;

@@ -91,6 +91,11 @@ bool decode_tc_eligible(const DecodeCall &c, const DecodePlan &p);
 sffn_status run_decode_tc(const DecodeCall &c, const DecodePlan &p, cudaStream_t s, bool dense);
 // One-token int4 decode on the CUDA cores (decode_q1.cu); dense = every neuron.
 bool decode_q1_eligible(const DecodeCall &c, const DecodePlan &p, bool dense);
+// Gate-and-up scores (with a_j and u_j) of one token with int4-g64 weights
+// (decode_q1.cu): the keep-ratio rule's first step.
+bool scores_q1_eligible(const sffn_ffn_weights *w, const DecodePlan &p);
+cudaError_t run_scores_q1(const sffn_ffn_weights *w, const void *x, const DecodePlan &p, float *score, float *aeff,
+                          float *uval, cudaStream_t s);
 sffn_status run_decode_q1(const DecodeCall &c, const DecodePlan &p, cudaStream_t s, bool dense);
 sffn_status run_down_norms(const sffn_ffn_weights *w, float *norms, cudaStream_t s);
 // One-token finish over per-chunk partials and lists in the workspace (part
