@@ -312,3 +312,31 @@ def test_dense_layer_matches_oracle(sffn, case):
     ref = O.decode(ffn_from_layer(layer), mat_from_act(x), O.THRESHOLD, O.SCORE_GATE, 0.0, nthreads=16)
     assert (ref["n_active"] == F).all()
     check_outputs(out.float().cpu().numpy().astype(np.float64), ref["out"], TOL[wd])
+
+
+# sffn_gate_scores: the per-neuron scores themselves against the oracle's, within
+# 1e-5 of the oracle's bound on the score computation (cond).  One token with
+# int4 weights and the gate-and-up score runs the int4 score stream; the other
+# cases the gate kernel.
+@pytest.mark.parametrize("cfg,wd,B", [(4, "int4_g64", 1), (4, "int4_g64", 3), (3, "bf16", 1)],
+                         ids=["int4-B1", "int4-B3", "bf16-B1"])
+@pytest.mark.parametrize("score", ["gate", "gate_up"])
+def test_gate_scores_match_the_oracle(sffn, cfg, wd, B, score):
+    from tests.oracle_io import ffn_from_layer, mat_from_act
+    from tests.parity import layer_to
+    import oracle as O
+    d, F = 1024, 1500
+    layer = W.make_ffn_layer(cfg, seed=57, d_model=d, d_ff=F, wdtype=wd)
+    x = W.make_tokens(cfg, B, seed=57, d_model=d)
+    w = sffn.Weights(layer_to(layer, "cuda"))
+    w.set_down_norms(sffn.down_norms(w))
+    kind = sffn.SCORE_GATE if score == "gate" else sffn.SCORE_GATE_UP
+    sc = sffn.gate_scores(x.cuda(), w, kind)
+    torch.cuda.synchronize()
+    ref = O.decode(ffn_from_layer(layer), mat_from_act(x), O.THRESHOLD,
+                   O.SCORE_GATE if score == "gate" else O.SCORE_GATE_UP, 0.0, details=True, nthreads=8)
+    got = sc.cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref["score"])
+    bound = 1e-5 * ref["cond"] + 1e-12
+    assert (err <= bound).all(), f"max err / cond {np.max(err / (ref['cond'] + 1e-30)):.3e}"
+    assert np.all(got >= 0.0)
