@@ -602,13 +602,70 @@ __global__ void __launch_bounds__(kSelThreads) k_keep_ratio(KeepArgs a) {
         forced = fmask;
     }
     const TopkCut cut = radix_topk(key, F, kk, forced, hist, tmp);
-    TopkChunk ch = topk_chunk(key, F, forced, cut, tmp);
 
     const bool want_h = a.lh && a.nb == 1;  // h_j = a_j * u_j for the selected neurons
     // a_j outside the selection is read only through the union of B > 1 tokens
     const bool zero_rest = a.nb > 1;
     float *aeff = a.aeff + (size_t)b * F;
     int32_t *lidx = a.lidx + (size_t)b * F;
+    if (key == skey && cut.take_eq == cut.n_eq) {
+        // Every candidate equal to the cut is taken (no tie straddles it), so the
+        // selection is key >= T or forced and needs no count of the keys before a
+        // warp's chunk: one pass ranks each warp's selections into its own,
+        // already-read stretch of the staged keys; then the warps' offsets, and
+        // the lists and h_j are written with all their loads in flight.
+        __shared__ int wtot[32];
+        const int warp = tid >> 5, nw = blockDim.x >> 5;
+        const int wchunk = (nwords + nw - 1) / nw;
+        const int w0 = min(nwords, warp * wchunk), w1 = min(nwords, w0 + wchunk);
+        uint32_t *buf = skey + 32 * w0;
+        const unsigned lt = (1u << lane) - 1u;
+        int nsel = 0;
+        for (int w = w0; w < w1; ++w) {
+            const int j = 32 * w + lane;
+            const bool ok = j < F;
+            const uint32_t kv = ok ? skey[j] : 0u;
+            const bool sel = ok && (bit_at(forced, j) || kv >= cut.T);
+            const unsigned bal = __ballot_sync(0xffffffffu, sel);
+            __syncwarp();  // every lane has read this word's key before any is overwritten
+            if (sel) buf[nsel + __popc(bal & lt)] = (uint32_t)j;
+            else if (zero_rest && ok) aeff[j] = 0.f;
+            nsel += __popc(bal);
+            if (lane == 0 && a.mask) a.mask[(size_t)b * nwords + w] = bal;
+        }
+        if (lane == 0) wtot[warp] = nsel;
+        __syncthreads();
+        int off = 0, total = 0;
+        for (int v = 0; v < nw; ++v) {
+            off += v < warp ? wtot[v] : 0;
+            total += wtot[v];
+        }
+        constexpr int UC = 4;
+        for (int i0 = 0; i0 < nsel; i0 += 32 * UC) {
+            int jj[UC];
+            float av[UC], uv[UC];
+#pragma unroll
+            for (int q = 0; q < UC; ++q) {
+                const int i = i0 + 32 * q + lane;
+                jj[q] = i < nsel ? (int)buf[i] : -1;
+            }
+#pragma unroll
+            for (int q = 0; q < UC; ++q) {
+                av[q] = want_h && jj[q] >= 0 ? aeff[jj[q]] : 0.f;
+                uv[q] = want_h && jj[q] >= 0 ? a.uval[jj[q]] : 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < UC; ++q) {
+                const int i = i0 + 32 * q + lane;
+                if (jj[q] < 0) continue;
+                lidx[off + i] = jj[q];
+                if (want_h) a.lh[off + i] = av[q] * uv[q];
+            }
+        }
+        for (int c = tid; c < a.C; c += blockDim.x) a.cnt[(size_t)b * a.C + c] = c == 0 ? total : 0;
+        return;
+    }
+    TopkChunk ch = topk_chunk(key, F, forced, cut, tmp);
     constexpr int U = 4;  // mask words per step: their selections first, then the a_j, u_j loads together
     for (int w = ch.w0; w < ch.w1; w += U) {
         TopkWord t[U];

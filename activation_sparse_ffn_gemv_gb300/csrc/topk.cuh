@@ -63,15 +63,16 @@ SFFN_DEV bool bit_at(const uint32_t *mask, int j) { return mask && ((mask[j >> 5
 struct TopkCut {
     uint32_t T;        // the k-th largest candidate key
     unsigned take_eq;  // candidates equal to T that are taken, lowest index first
+    unsigned n_eq;     // candidates equal to T (take_eq == n_eq: every one of them is taken)
 };
 
 // The cut of the k largest candidate keys (k <= the number of candidates);
 // k == 0 selects no candidate.
 SFFN_DEV TopkCut radix_topk(const uint32_t *key, int F, unsigned k, const uint32_t *forced, unsigned *hist,
                             int *tmp) {
-    if (k == 0) return TopkCut{0xFFFFFFFFu, 0u};
+    if (k == 0) return TopkCut{0xFFFFFFFFu, 0u, 0u};
     uint32_t prefix = 0, pmask = 0;
-    unsigned need = k;
+    unsigned need = k, n_eq = 0;
     const int shifts[3] = {21, 10, 0};
     const int widths[3] = {11, 11, 10};
     for (int pass = 0; pass < 3; ++pass) {
@@ -88,8 +89,9 @@ SFFN_DEV TopkCut radix_topk(const uint32_t *key, int F, unsigned k, const uint32
         prefix |= (uint32_t)bin << sh;
         pmask |= (uint32_t)(nbins - 1) << sh;
         need -= above;
+        if (pass == 2) n_eq = hist[bin];  // the last digit: the bin holds exactly the keys equal to T
     }
-    return TopkCut{prefix, need};
+    return TopkCut{prefix, need, n_eq};
 }
 
 // This warp's chunk of 32-key words [w0, w1) for the ordered pass, with the
