@@ -743,7 +743,30 @@ struct UpDownArgs {
     float *part;               // [G2, nb, d]
     int32_t *active_idx;       // nb == 1: the walked list is the token's own list; write it here
     int32_t *n_active;
+    unsigned *gbar;            // non-null: finish the call here (grid barrier, sum of the partials)
+    void *out;
+    int out_f32;
+    int32_t *err;
 };
+
+// The end of a keep-ratio call inside its down kernel: every CTA is resident
+// (grid <= #SMs) and the token's list is already written, so the CTAs meet at
+// the grid barrier and sum the partials (decode_finish.cuh) without a list.
+template <class A>
+SFFN_DEV void finish_partials(const A &a, int d, unsigned bar_base) {
+    FinishArgs fa = {};
+    fa.gbar = a.gbar;
+    fa.part = a.part;
+    fa.nb = a.nb;
+    fa.d = d;
+    fa.F = a.F;
+    fa.C = a.C;
+    fa.R = a.R;
+    fa.out = a.out;
+    fa.out_f32 = a.out_f32;
+    fa.err = a.err;
+    finish_call(fa, bar_base, false);
+}
 
 constexpr int kMaxC = 2048;     // max gate CTAs (chunks)
 constexpr int kListChunks = 8;  // chunks per list-writing CTA of the reduction
@@ -770,6 +793,7 @@ __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
     stage_x<W>(xs, a.x, a.nb, NB, d);
     griddep_wait();
     griddep_launch_dependents();
+    const unsigned bar_base = a.gbar ? *reinterpret_cast<volatile unsigned *>(a.gbar + 1) : 0u;
 
     // exclusive scan of the walked list's chunk counts
     const int *cnt = a.cnt + (size_t)a.list_u * a.C;
@@ -899,6 +923,7 @@ __global__ void __launch_bounds__(kUpDownMaxThreads) k_updown(UpDownArgs a) {
             }
         }
     }
+    if (a.gbar) finish_partials(a, d, bar_base);
 }
 
 // ---------------------------------------------------------------------------
@@ -921,7 +946,13 @@ struct DownArgs {
     float *part;               // [G2, nb, d]
     int32_t *active_idx;       // nb == 1: write the token's list here
     int32_t *n_active;
+    unsigned *gbar;            // non-null: finish the call here (grid barrier, sum of the partials)
+    void *out;
+    int out_f32;
+    int32_t *err;
 };
+
+
 
 constexpr int kDownMaxThreads = 512;
 
@@ -941,6 +972,7 @@ __global__ void __launch_bounds__(kDownMaxThreads) k_down(DownArgs a) {
 
     griddep_wait();
     griddep_launch_dependents();
+    const unsigned bar_base = a.gbar ? *reinterpret_cast<volatile unsigned *>(a.gbar + 1) : 0u;
     const int *cnt = a.cnt + (size_t)a.list_u * a.C;
     const int *lidx = a.lidx + (size_t)a.list_u * F;
     int nr;
@@ -1048,6 +1080,7 @@ __global__ void __launch_bounds__(kDownMaxThreads) k_down(DownArgs a) {
             }
         }
     }
+    if (a.gbar) finish_partials(a, d, bar_base);
 }
 
 // ---------------------------------------------------------------------------
@@ -1265,6 +1298,7 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
 
     int nparts = p.G2;
     bool list_ctas = p.nb > 1;
+    bool fin_down = false;
     if (!keep) {  // exact / threshold: the gate kernel already wrote per-chunk partials
         nparts = p.C;
         list_ctas = true;
@@ -1305,6 +1339,11 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
 
         const int threads = ((p.d / 8) + 31) / 32 * 32;
         const int max_rows = (p.F + p.G2 - 1) / p.G2 + 1;
+        // keep-ratio with one token: the token's list is written by the select and
+        // the down kernel, so the down kernel can finish the call itself (its CTAs
+        // are all resident and at least 256 threads wide)
+        fin_down = keep && p.nb == 1 && threads >= 256 && nparts <= device_sm_count();
+        unsigned *gbar = fin_down ? reinterpret_cast<unsigned *>(ws + p.off_err + kCtlBar) : nullptr;
         if (!keep) {
             // nothing between the gate kernel and the reduction
         } else if (have_h) {
@@ -1325,6 +1364,10 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
             da.n_active = p.nb == 1 ? c.n_active : nullptr;
             da.by_chunk = 0;  // keep-ratio lists are one block, not per gate chunk
             da.max_rows = max_rows;
+            da.gbar = gbar;
+            da.out = c.out;
+            da.out_f32 = w->wdtype == SFFN_F32;
+            da.err = err;
             const size_t smem = sizeof(int) * (kMaxC + 1 + da.max_rows) + sizeof(float) * (size_t)da.max_rows * NB;
             e = set_max_smem((const void *)k_down<W, NB>, (int)smem);
             if (e == cudaSuccess) e = launch_k(k_down<W, NB>, dim3(nparts), dim3(threads), smem, s, da);
@@ -1348,12 +1391,17 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
             ua.part = part;
             ua.active_idx = p.nb == 1 ? c.active_idx : nullptr;
             ua.n_active = p.nb == 1 ? c.n_active : nullptr;
+            ua.gbar = gbar;
+            ua.out = c.out;
+            ua.out_f32 = w->wdtype == SFFN_F32;
+            ua.err = err;
             const size_t smem = sizeof(float) * NB * p.d + sizeof(int) * (kMaxC + 1 + max_rows);
             e = set_max_smem((const void *)k_updown<W, NB, false>, (int)smem);
             if (e == cudaSuccess) e = launch_k(k_updown<W, NB, false>, dim3(p.G2), dim3(threads), smem, s, ua);
         }
         if (e != cudaSuccess) return e;
     }
+    if (fin_down) return cudaSuccess;
 
     ReduceArgs ra = {};
     ra.part = part;
