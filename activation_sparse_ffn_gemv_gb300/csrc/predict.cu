@@ -27,6 +27,7 @@
 #include <cmath>
 
 #include "common.cuh"
+#include "decode_finish.cuh"
 #include "internal.h"
 #include "wformat.cuh"
 
@@ -135,6 +136,10 @@ struct LrArgs {
     float alpha;
     int *cnt, *lidx;    // [C], [C, R]: the chunk's active neurons, ascending
     float *part;        // [C, d]: the chunk's partial output
+    unsigned *gbar;     // non-null: every chunk's CTA is resident; finish the call here
+    void *out;
+    int out_f32;
+    int32_t *active_idx, *n_active;
 };
 
 constexpr int kLrMaxUnits = 4;  // 16-byte units of a W_downT row per thread (d_model <= 4096)
@@ -173,10 +178,13 @@ __global__ void __launch_bounds__(kLrThreads) k_lr_ffn(LrArgs a) {
         // A is an input of the call: stream it before waiting for y
         for (int k = 0; k < min(2, npieces); ++k) issue(k);
     }
-    // x is an input of the call, never written by its kernels
-    stage_x<W>(xs, a.x, 1, 1, a.d);
+    // x may be the previous call's output: with the projection kernel in front
+    // (which waited for that call) it can be read now; otherwise only after the wait
+    if (!a.all) stage_x<W>(xs, a.x, 1, 1, a.d);
     griddep_wait();
     griddep_launch_dependents();
+    if (a.all) stage_x<W>(xs, a.x, 1, 1, a.d);
+    const unsigned bar_base = a.gbar ? *reinterpret_cast<volatile unsigned *>(a.gbar + 1) : 0u;
 
     // ---- predicted pre-activations and candidates
     if (a.all) {
@@ -343,6 +351,26 @@ __global__ void __launch_bounds__(kLrThreads) k_lr_ffn(LrArgs a) {
             for (int e = 0; e < W::E; e += 4) d4[e / 4] = make_float4(acc[k][e], acc[k][e + 1], acc[k][e + 2], acc[k][e + 3]);
         }
     }
+    if (a.gbar) {
+        // the grid barrier, the fixed-order sum of the chunks' partials and the
+        // token's list (decode_finish.cuh), as the gate kernel ends an exact call
+        FinishArgs fa = {};
+        fa.gbar = a.gbar;
+        fa.part = a.part;
+        fa.nb = 1;
+        fa.d = a.d;
+        fa.F = a.F;
+        fa.C = gridDim.x;
+        fa.R = a.R;
+        fa.cnt = a.cnt;
+        fa.lidx = a.lidx;
+        fa.out = a.out;
+        fa.out_f32 = a.out_f32;
+        fa.active_idx = a.active_idx;
+        fa.n_active = a.n_active;
+        fa.err = a.err;
+        finish_call(fa, bar_base, false);
+    }
 }
 
 template <class W>
@@ -373,6 +401,14 @@ cudaError_t predicted_t(const DecodeCall &c, const DecodePlan &p, const float *f
     la.cnt = reinterpret_cast<int *>(ws + p.off_cnt);
     la.lidx = reinterpret_cast<int *>(ws + p.off_lidx);
     la.part = reinterpret_cast<float *>(ws + p.off_part);
+    // every chunk's CTA resident: the kernel finishes the call itself
+    if (p.C <= device_sm_count()) {
+        la.gbar = reinterpret_cast<unsigned *>(ws + p.off_err + kCtlBar);
+        la.out = c.out;
+        la.out_f32 = c.w->wdtype == SFFN_F32;
+        la.active_idx = c.active_idx;
+        la.n_active = c.n_active;
+    }
     // A's rows stream in bulk pieces when every row starts on a 16-byte boundary
     const bool bulk = !all && rank % 4 == 0 && (reinterpret_cast<uintptr_t>(fa) & 15u) == 0;
     la.piece_rows = 0;
@@ -399,6 +435,7 @@ sffn_status run_decode_predicted(const DecodeCall &c, const DecodePlan &p, const
     default: return SFFN_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return SFFN_ERR_CUDA;
+    if (p.C <= device_sm_count()) return SFFN_OK;  // k_lr_ffn finished the call
     return run_reduce_chunks(c, p, s);
 }
 
