@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gate_tc(TcArgs a) {
     float *hs = sa + kTcMaxRows * kTcN;                                    // h per (union position, token)
     int *urow = reinterpret_cast<int *>(hs + kTcMaxRows * kTcN);          // union rows, ascending
     __shared__ uint32_t sflag[kTcMaxRows];
+    __shared__ float sbias[kTcMaxRows], snorm[kTcMaxRows];
     __shared__ int wcnt[kTcN + 1][4];
     __shared__ int slot_rel[kTcMaxSlots];   // warps done with the slot's current stage
     __shared__ int slot_iss[kTcMaxSlots];   // stages issued into the slot
@@ -160,6 +161,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gate_tc(TcArgs a) {
     const int ngs = (nrows + kTcStageRows - 1) / kTcStageRows;  // gate stages
 
     if (tid < kTcMaxRows) sflag[tid] = 0u;
+    // the gate bias of the chunk's rows: an input, like the weights
+    if (tid < nrows) sbias[tid] = a.bias ? __ldg(a.bias + row0 + tid) : 0.f;
     if (tid < kTcMaxSlots) slot_rel[tid] = slot_iss[tid] = 0;
     if (tid == 0) {
         s_abort = 0;
@@ -224,6 +227,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gate_tc(TcArgs a) {
     griddep_wait();
     griddep_launch_dependents();
     const unsigned bar_base = *reinterpret_cast<volatile unsigned *>(a.gbar + 1);
+    // the rows' ||W_down[:, j]|| (threshold rule; they may come from the previous
+    // kernel), in shared memory long before the decision reads them
+    if (tid < nrows) snorm[tid] = !DENSE && a.mode != SFFN_MODE_EXACT && a.norms ? a.norms[row0 + tid] : 0.f;
 
     int ck = 0;  // stages consumed by this warp
     auto consume_wait = [&](int k) -> bool {
@@ -320,12 +326,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gate_tc(TcArgs a) {
             float gv = 0.f;
 #pragma unroll
             for (int w = 0; w < kTcCons; ++w) gv += gp[((size_t)w * kTcMaxRows + r) * kTcN + b];
-            if (a.bias) gv += a.bias[row0 + r];
+            gv += sbias[r];
             const float av = act_fn(a.act, gv);
             if (DENSE) {
                 sa[r * kTcN + b] = av;
             } else {
-                const bool active = a.mode == SFFN_MODE_EXACT ? av != 0.f : fabsf(av) * a.norms[row0 + r] >= a.tau;
+                const bool active = a.mode == SFFN_MODE_EXACT ? av != 0.f : fabsf(av) * snorm[r] >= a.tau;
                 sa[r * kTcN + b] = active ? av : 0.f;
                 if (active) atomicOr(&sflag[r], 1u << b);
             }
