@@ -291,6 +291,7 @@ DENSE = [
     (4, 2048, 11008, "int4_g64", "silu", 1),
     (4, 4096, 3000, "int4_g64", "silu", 1),
     (4, 512, 333, "int4_g64", "relu", 1),
+    (4, 1024, 700, "int4_g64", "silu", 1),
     (4, 1024, 700, "int4_g64", "silu", 3),
     (2, 4096, 11008, "bf16", "relu", 1),
     (3, 1024, 2050, "bf16", "silu", 8),
