@@ -23,6 +23,8 @@
 #include "topk.cuh"
 #include "wformat.cuh"
 
+#include <algorithm>
+
 namespace sffn {
 
 // ---------------------------------------------------------------------------
@@ -93,9 +95,13 @@ struct GateArgs {
     void *out;
     int out_f32;
     int32_t *active_idx, *n_active;
+    // the first pf_early CTAs send rows 0 .. pf_rows-1 of the later chunks to L2
+    // before their dependency wait (0: none)
+    int pf_early, pf_rows;
 };
 
 constexpr int kGateWarps = 8;           // each warp streams its own rows
+constexpr int kGatePfRows = 48;         // rows of each later chunk sent to L2 by the early CTAs
 constexpr int kGateThreads = 32 * kGateWarps;
 constexpr int kMaxChunk = 256;   // R <= kMaxChunk <= blockDim: one scan pass compacts a chunk
 constexpr int kMaxStages = 16;   // ring stages per warp
@@ -271,6 +277,26 @@ __global__ void __launch_bounds__(kGateThreads, 1) k_gate(GateArgs a) {
         s_abort = 0;
         mbar_init(dbar, 1);
         mbar_fence_init();
+    }
+    // When calls follow each other, the first CTAs of this call find free SMs
+    // (the previous call's CTAs that do not reduce have left) while the
+    // previous call's reducers still hold the others.  Those early CTAs send the
+    // first rows of the later chunks to L2, so that HBM streams through that
+    // gap and the later CTAs' first ring items are L2 hits.  Chunk c >= E is
+    // covered by early CTA c % E; the rows go out in row order across chunks.
+    if (a.pf_early > 0 && (int)blockIdx.x < a.pf_early && warp == kGateWarps - 1) {
+        const int E = a.pf_early;
+        const int nch = (a.C - 1 - (int)blockIdx.x) / E;  // chunks blockIdx.x + E m, m = 1 .. nch
+        const int P = min(a.pf_rows, a.R);
+        const char *wg = static_cast<const char *>(a.wg);
+        for (int i = lane; i < nch * P; i += 32) {
+            const int r = i / nch, c = (int)blockIdx.x + (1 + i % nch) * E;
+            const int j = c * a.R + r;
+            if (j < F) {
+                bulk_prefetch_l2(wg + (size_t)j * row_bytes, row_bytes);
+                if (W::Q) bulk_prefetch_l2(static_cast<const char *>(a.sg) + (size_t)j * sbytes, sbytes);
+            }
+        }
     }
     // x may be the previous layer's output: read it only after the dependency wait
     griddep_wait();
@@ -1231,6 +1257,15 @@ static cudaError_t launch_gate(const GateArgs &ga_in, const DecodePlan &p, cudaS
     if (D > rows_per_warp) D = rows_per_warp;
     if (D < 1) return cudaErrorInvalidConfiguration;
     ga.stages = (int)D;
+    if (ga.gbar && ga.pf_rows > 0) {
+        // CTAs that start before the previous call's reducers leave: the idle
+        // SMs plus the previous call's non-reducing CTAs (the reducer count of
+        // decode_finish.cuh for the same grid)
+        const long C = p.C, total = (long)p.nb * p.d;
+        const long NR = std::min(C, std::max((total + 31) / 32, (C + 3) / 4));
+        const int E = device_sm_count() - (int)NR;
+        ga.pf_early = E > 0 && E < p.C ? E : 0;
+    }
     const size_t smem = gate_smem(x_bytes, stage_bytes, ga.stages);
     e = set_max_smem((const void *)k_gate<W, NB, UP>, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1280,6 +1315,7 @@ static cudaError_t launch_decode_t(const DecodeCall &c, const DecodePlan &p, cud
     // the call itself (grid barrier + distributed reduction + index lists)
     const bool fused = !scores_only && !keep && p.C <= device_sm_count();
     ga.gbar = fused ? reinterpret_cast<unsigned *>(ws + p.off_err + kCtlBar) : nullptr;
+    ga.pf_rows = fused ? kGatePfRows : 0;
     ga.out = c.out;
     ga.out_f32 = w->wdtype == SFFN_F32;
     ga.active_idx = c.active_idx;
