@@ -19,6 +19,7 @@ struct FinishArgs {
     int out_f32;
     int32_t *active_idx, *n_active;
     int32_t *err;
+    int nr_cap = 0;  // > 0: at most this many reducers
 };
 
 // Called by all threads (>= 256) of every CTA of the call once the CTA's
@@ -43,7 +44,8 @@ SFFN_DEV unsigned ld_acquire(const unsigned *p) {
 SFFN_DEV void finish_call(const FinishArgs &a, unsigned bar_base, bool failed) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const size_t total = (size_t)a.nb * a.d;
-    const int NR = (int)min((size_t)gridDim.x, max((total + 31) / 32, (size_t)(gridDim.x + 3) / 4));
+    int NR = (int)min((size_t)gridDim.x, max((total + 31) / 32, (size_t)(gridDim.x + 3) / 4));
+    if (a.nr_cap > 0 && a.nr_cap < NR) NR = a.nr_cap;
     __shared__ int s_bar_ok;
     __shared__ float red[8][32];
     // The arrival is one release add at GPU scope after a CTA barrier: every

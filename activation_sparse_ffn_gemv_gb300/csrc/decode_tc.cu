@@ -42,12 +42,15 @@
 #include "decode_finish.cuh"
 #include "internal.h"
 
+#include <algorithm>
+
 namespace sffn {
 
 namespace {
 
 constexpr int kTcCons = 8;                   // warps: all consume every stage
 constexpr int kTcThreads = 32 * kTcCons;
+constexpr int kTcPfRows = 48;               // rows of each later chunk sent to L2 by the early CTAs
 constexpr int kTcMaxRows = 128;              // rows per chunk
 constexpr int kTcStageRows = 8;              // rows per stage: the MMA's N
 constexpr int kTcMaxSlots = 16;
@@ -68,6 +71,8 @@ struct TcArgs {
     unsigned *gbar;
     void *out;
     int32_t *active_idx, *n_active;
+    int nr_cap;                // reducers of the finish (fewest with the same load rounds)
+    int pf_early, pf_rows;     // the first pf_early CTAs send rows 0 .. pf_rows-1 of the later chunks to L2
 };
 
 // D += A * B, m16n8k16 / m16n8k8, bf16 inputs, fp32 accumulators.
@@ -223,6 +228,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gate_tc(TcArgs a) {
     };
     // The weights are constant inputs: the first stages move before the wait
     for (int j = warp; j < NS && j < s_known; j += kTcCons) issue_stage(j);
+    // The first CTAs of a call find free SMs while the previous call's reducers
+    // still hold the others; they send the first gate rows of the later chunks
+    // (chunk c >= E to CTA c mod E, row order across chunks) to L2, so that HBM
+    // streams through the previous call's finish.
+    if (a.pf_early > 0 && (int)blockIdx.x < a.pf_early && warp == kTcCons - 1) {
+        const int E = a.pf_early;
+        const int nch = (a.C - 1 - (int)blockIdx.x) / E;
+        const int P = min(a.pf_rows, a.R);
+        for (int i = lane; i < nch * P; i += 32) {
+            const int r = i / nch, c = (int)blockIdx.x + (1 + i % nch) * E;
+            const int jr = c * a.R + r;
+            if (r < a.R && jr < F) {
+                bulk_prefetch_l2(a.wg + (size_t)jr * row_bytes, row_bytes);
+                if (Q) bulk_prefetch_l2(a.sg + (size_t)jr * sbytes, sbytes);
+            }
+        }
+    }
     // x may be the previous layer's output: read it only after the dependency wait
     griddep_wait();
     griddep_launch_dependents();
@@ -492,6 +514,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gate_tc(TcArgs a) {
     fa.active_idx = a.active_idx;
     fa.n_active = a.n_active;
     fa.err = a.err;
+    fa.nr_cap = a.nr_cap;
     finish_call(fa, bar_base, s_abort != 0);
 }
 
@@ -505,6 +528,23 @@ cudaError_t launch_tc(TcArgs ta, const DecodePlan &p, cudaStream_t s) {
     if (slots > need) slots = need;
     if (slots < 2) return cudaErrorInvalidConfiguration;
     ta.slots = (int)slots;
+    {
+        // When the finish takes at most two rounds of 32-column blocks (two
+        // blocks per round), only the fewest reducers that keep that many
+        // rounds wait at the barrier; the other CTAs leave, and as many CTAs
+        // of the next call start early (with the idle SMs) and prefetch.  With
+        // more rounds every CTA reduces (measured: capping them at B = 8 made
+        // the call slower).
+        const long C = p.C, nblk = ((long)p.nb * p.d + 31) / 32, minr = (C + 3) / 4;
+        const long nr0 = std::min(C, std::max(nblk, minr));
+        const long rounds = (nblk + 2 * nr0 - 1) / (2 * nr0);
+        const bool cap = rounds <= 2;
+        const long nr = cap ? std::min(nr0, std::max((nblk + 2 * rounds - 1) / (2 * rounds), minr)) : nr0;
+        ta.nr_cap = (int)nr;
+        const long E = (long)device_sm_count() - nr;
+        ta.pf_early = cap && E > 0 && E < C ? (int)E : 0;
+        ta.pf_rows = kTcPfRows;
+    }
     const size_t smem = tc_smem_bytes(d, Q, (int)slots);
     cudaError_t e = set_max_smem((const void *)k_gate_tc<Q, NU, DENSE>, (int)smem);
     if (e != cudaSuccess) return e;
