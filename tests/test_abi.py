@@ -124,6 +124,32 @@ def test_noalloc_reports_argument_errors_like_decode(S):
     assert L.sffn_decode_noalloc_read_error(None, None) == S.ERR_INVALID_ARG
 
 
+def test_gate_scores_argument_checks(S):
+    # sffn_gate_scores takes the decode's checks for the threshold rule (down
+    # norms required) and its own scores pointer, all before any CUDA call
+    L = S.lib()
+
+    def wts(norms=16, **kw):
+        f = dict(wdtype=S.BF16, act=S.ACT_SILU, d_model=512, d_ff=128)
+        f.update(kw)
+        return S.FFNWeights(f["wdtype"], f["act"], f["d_model"], f["d_ff"], 16, 16, 16, 16, 16, 16, None, norms)
+
+    def gs(w, B=1, score=0, x=16, scores=16):
+        return L.sffn_gate_scores(x, B, C.byref(w), score, scores, 256, 1 << 20, None)
+
+    assert gs(wts(), x=None) == S.ERR_INVALID_ARG
+    assert gs(wts(), scores=None) == S.ERR_INVALID_ARG
+    assert gs(wts(), score=5) == S.ERR_INVALID_ARG
+    assert gs(wts(norms=None)) == S.ERR_INVALID_ARG   # the score needs ||W_down[:, j]||
+    assert gs(wts(norms=8)) == S.ERR_ALIGNMENT
+    assert gs(wts(), B=0) == S.ERR_SHAPE
+    assert gs(wts(), B=9) == S.ERR_SHAPE
+    assert gs(wts(d_model=8192)) == S.ERR_SHAPE
+    assert gs(wts(wdtype=S.INT4_G64, d_model=576)) == S.ERR_SHAPE  # int4 rows: d % 512
+    assert gs(wts(), x=8) == S.ERR_ALIGNMENT
+    assert L.sffn_gate_scores(16, 1, None, 0, 16, 256, 1 << 20, None) == S.ERR_INVALID_ARG
+
+
 def test_dense_layer_argument_checks(S):
     L = S.lib()
 
